@@ -1,0 +1,61 @@
+// Internal interface between the host planner / C ABI (exact_topk_api.cpp)
+// and the kernel translation unit (topk_kernels.cu).  Not installed.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime_api.h>
+
+#include "exact_topk.h"
+
+namespace etk {
+
+// Counter buffer layout (int32 words).  The queue head and exit counter drive
+// the persistent row queue; arrive[r] elects the KV-split finisher of row r;
+// status is a sticky error word that stays zero unless a device-side bounds
+// guard tripped.  Every launch returns words 0, 1 and arrive[] to zero.
+constexpr int kCtrQueue = 0;
+constexpr int kCtrExit = 1;
+constexpr int kCtrStatus = 2;
+constexpr int kCtrArriveBase = 4;
+
+constexpr int kPersistentThreads = 512;
+constexpr int kKvSplitThreads = 512;
+constexpr int kRowLocalThreads = 1024;
+constexpr int kPersistentCap = 4096;
+constexpr int kKvSplitCap = 4096;
+constexpr int kRowLocalCap = 8192;
+// Rows of the row-local exact kernel up to this length stay in registers.
+constexpr int kRowLocalResident = 8 * kRowLocalThreads;
+
+struct LaunchArgs {
+  const float* logits;
+  const int32_t* ke;
+  int32_t* out;
+  const int32_t* num_valid_rows;
+  void* counters;
+  void* workspace;
+  const int32_t* prev_topk;
+  int32_t* trace;
+};
+
+// Bytes of dynamic shared memory a kernel of `family` uses for a frontier of
+// `cap` entries.
+size_t shared_bytes(int family, int cap);
+
+// Workspace carve-up shared by the planner and the launcher.
+struct WorkspaceLayout {
+  uint64_t idx_offset;    // int32 [slices][N]
+  uint64_t key_offset;    // uint32 [slices][N]
+  uint64_t seg_offset;    // int32 pairs [M][P] (KV-split published counts)
+  uint64_t total;
+  int64_t slices;
+};
+WorkspaceLayout workspace_layout(const exact_topk_plan& plan);
+
+// Implemented in topk_kernels.cu.
+int kernel_occupancy(int family, int device, int* ctas_per_sm);
+int launch(const exact_topk_plan& plan, const LaunchArgs& args, cudaStream_t stream);
+
+}  // namespace etk

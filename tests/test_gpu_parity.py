@@ -1,0 +1,266 @@
+"""GPU parity of the CUDA path (through the C ABI) against the CPU oracle.
+
+The bar: bit-exact multisets of selected FP32 values per row (ties at rank K
+may pick different indices), exactness criterion eq. 30 of section 6.1, the
+-1 pad rule of section 2.1, untouched rows beyond the live count, counters
+restored to zero, and the per-row route trace (Table 2 of section 4.6)
+identical to the oracle's written-out method.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import exact_top_selection_gb300 as etk
+import oracle
+import workloads
+from gpu_helpers import (CANARY, assert_counters_zero, compare_rows, compare_trace,
+                         oracle_trace_for_plan, run_gpu)
+
+pytestmark = pytest.mark.gpu
+
+FAMILIES = [etk.FAMILY_PERSISTENT_SAMPLED, etk.FAMILY_KV_SPLIT, etk.FAMILY_ROW_LOCAL_EXACT]
+
+
+def _rows(M, N, seed, dist):
+    X = workloads.iid_rows(M, N, seed, dist=dist).numpy()
+    return X
+
+
+def _ke(M, N, K, seed):
+    rng = np.random.default_rng(seed)
+    ke = rng.integers(0, N + 1, M).astype(np.int32)
+    special = [0, 1, K - 1, K, K + 1, N, N + 5, -3]
+    for i, v in enumerate(special[:M]):
+        ke[i] = v
+    return ke
+
+
+@pytest.mark.parametrize("family", FAMILIES)
+@pytest.mark.parametrize("N,K", [(1, 1), (7, 4), (64, 1), (4095, 256), (8191, 7), (8192, 256),
+                                 (12345, 2048), (40000, 2048)])
+def test_small_shapes_every_family(family, N, K):
+    M = 24
+    X = _rows(M, N, 1000 + N + K, "normal")
+    ke = _ke(M, N, K, N * 7 + K)
+    out, tr, plan, ctr = run_gpu(X, ke, K, family=family, stride=16 if N < 20000 else 0)
+    compare_rows(X, ke, K, out)
+    assert_counters_zero(ctr)
+    _, tr_ref = oracle_trace_for_plan(X, ke, K, plan)
+    compare_trace(tr, tr_ref)
+
+
+@pytest.mark.parametrize("family", FAMILIES)
+@pytest.mark.parametrize("dist", ["int", "uniform"])
+def test_tie_heavy_rows(family, dist):
+    M, N, K = 20, 30000, 2048
+    X = _rows(M, N, 77, dist)
+    ke = _ke(M, N, K, 78)
+    out, tr, plan, ctr = run_gpu(X, ke, K, family=family)
+    compare_rows(X, ke, K, out)
+    assert_counters_zero(ctr)
+    _, tr_ref = oracle_trace_for_plan(X, ke, K, plan)
+    compare_trace(tr, tr_ref)
+
+
+@pytest.mark.parametrize("name", workloads.ORDER)
+@pytest.mark.parametrize("family", [0] + FAMILIES)
+def test_scaled_workloads(name, family):
+    # The five workload recipes at sizes the oracle finishes in seconds, still
+    # spanning several tiles and a ragged tail.
+    w = workloads.WORKLOADS[name]
+    M = min(w.M, 48)
+    N = min(w.N, 40000 if w.N > 8192 else w.N)
+    K = min(w.K, 1024)
+    Xt, ket, K = workloads.generate(name, M=M, N=N, K=K, device="cpu")
+    X, ke = Xt.numpy(), ket.numpy()
+    out, tr, plan, ctr = run_gpu(X, ke, K, family=family)
+    compare_rows(X, ke, K, out)
+    assert_counters_zero(ctr)
+    _, tr_ref = oracle_trace_for_plan(X, ke, K, plan)
+    compare_trace(tr, tr_ref)
+
+
+@pytest.mark.parametrize("family", [etk.FAMILY_PERSISTENT_SAMPLED, etk.FAMILY_KV_SPLIT])
+@pytest.mark.parametrize("dual", [0, 1])
+def test_forced_routes(family, dual):
+    # Table 2's routes, forced by planting large values on or off the sampled
+    # residue class (the view phase is a pure function of the row, eq. 13).
+    K, s, N = 64, 16, 8192
+    q0 = -(-3 * K // (2 * s))
+    q1 = -(-7 * K // (4 * s))
+    rng = np.random.default_rng(8)
+    base = rng.standard_normal(N).astype(np.float32)
+
+    def planted(r, off_hi, off_mid):
+        row = base.copy()
+        a = oracle.view_phase(r, s)
+        on = np.arange(a, N, s)
+        off = np.array([i for i in range(N) if i % s != a])
+        row[on[:q0]] = 100.0
+        row[on[q0:q1]] = 90.0
+        row[off[:off_hi]] = 100.0
+        row[off[off_hi:off_hi + off_mid]] = 90.0
+        return row
+
+    X = np.stack([base, planted(1, 30, 50), planted(2, 30, 0), base])
+    ke = np.array([N, N, N, 100], np.int32)
+    out, tr, plan, ctr = run_gpu(X, ke, K, family=family, stride=s, dual=dual, splits=3)
+    compare_rows(X, ke, K, out)
+    assert_counters_zero(ctr)
+    _, tr_ref = oracle_trace_for_plan(X, ke, K, plan)
+    compare_trace(tr, tr_ref)
+    if dual:
+        assert tr[:, 0].tolist() == [1, 2, 3, 5]
+    else:
+        assert tr[:3, 0].tolist() == [1, 4, 4]
+
+
+@pytest.mark.parametrize("family", [etk.FAMILY_PERSISTENT_SAMPLED, etk.FAMILY_KV_SPLIT])
+def test_guess_source(family):
+    M, N, K = 12, 20000, 512
+    X = _rows(M, N, 5, "normal")
+    ke = np.full(M, N, np.int32)
+    ke[7] = 300
+    ref = oracle.topk_rows(X, ke, K)
+    guess = ref.copy()
+    rng = np.random.default_rng(3)
+    guess[1] = rng.permutation(N)[:K]        # poor but valid
+    guess[2, 5] = -1                          # invalid entry -> sampled route
+    guess[3] = np.argmax(X[3])                # K copies of one index -> exact recovery
+    guess[4, :] = np.arange(K)                # arbitrary valid
+    guess[5, 0] = N + 10                      # out of range -> sampled route
+    guess[7] = 0                              # pad row ignores the guess
+    out, tr, plan, ctr = run_gpu(X, ke, K, prev=guess, family=family)
+    compare_rows(X, ke, K, out, ref=ref)
+    assert_counters_zero(ctr)
+    _, tr_ref = oracle_trace_for_plan(X, ke, K, plan, prev=guess)
+    compare_trace(tr, tr_ref)
+    assert tr[0, 0] == 6 and tr[3, 0] == 7
+
+
+@pytest.mark.parametrize("family", FAMILIES)
+def test_live_rows_and_canary(family):
+    M, N, K = 16, 9000, 100
+    X = _rows(M, N, 11, "normal")
+    ke = np.full(M, N, np.int32)
+    for m_live in (0, 1, 9, 16, 40):
+        out, tr, plan, ctr = run_gpu(X, ke, K, num_valid=m_live, family=family)
+        eff = min(max(m_live, 0), M)
+        compare_rows(X, ke, K, out, M_live=eff)
+        assert (tr[eff:] == CANARY).all()
+        assert_counters_zero(ctr)
+
+
+@pytest.mark.parametrize("family", FAMILIES)
+@pytest.mark.parametrize("pitch_extra,offset", [(1, 0), (3, 1), (0, 2)])
+def test_unaligned_rows(family, pitch_extra, offset):
+    # Rows at a pitch that is not a multiple of 4 floats, and a base pointer
+    # that is only 4-byte aligned: scalar head/tail plus 128-bit body.
+    M, N, K = 10, 20001, 300
+    pitch = N + pitch_extra
+    rng = np.random.default_rng(pitch_extra * 10 + offset)
+    flat = rng.standard_normal(M * pitch + offset).astype(np.float32)
+    dev = torch.device("cuda")
+    flat_d = torch.as_tensor(flat).to(dev)
+    Xd = flat_d[offset:offset + M * pitch].view(M, pitch)[:, :N]
+    X = Xd.cpu().numpy()
+    ke = _ke(M, N, K, 5)
+    out, tr, plan, ctr = run_gpu(Xd, ke, K, row_pitch=pitch, family=family)
+    compare_rows(X, ke, K, out)
+    assert_counters_zero(ctr)
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 5, 64])
+def test_kv_split_counts(splits):
+    M, N, K = 6, 70000, 2048
+    Xt, ket, K = workloads.generate("long_decode", M=M, N=N, K=K)
+    X, ke = Xt.numpy(), ket.numpy()
+    out, tr, plan, ctr = run_gpu(X, ke, K, family=etk.FAMILY_KV_SPLIT, splits=splits)
+    assert plan.splits == splits
+    compare_rows(X, ke, K, out)
+    assert_counters_zero(ctr)
+    _, tr_ref = oracle_trace_for_plan(X, ke, K, plan)
+    compare_trace(tr, tr_ref)
+
+
+@pytest.mark.parametrize("family", FAMILIES)
+def test_frontier_spill_constant_and_tie_rows(family):
+    # Constant rows and huge tie bands push |Q0| to L, beyond on-chip capacity,
+    # through the global frontier slices.
+    M, N, K = 8, 60000, 2048
+    X = np.zeros((M, N), np.float32)
+    X[0] = 0.5
+    X[1] = np.where(np.arange(N) % 3 == 0, 2.0, 1.0)
+    X[2, :] = -np.inf
+    X[3] = np.float32(1e-40)
+    X[4] = np.where(np.arange(N) % 2 == 0, -0.0, 0.0)
+    X[5] = (np.arange(N) % 7).astype(np.float32)
+    X[6, :5000] = 3.0
+    X[7] = np.random.default_rng(1).integers(0, 2, N).astype(np.float32)
+    ke = np.array([N, N, N - 1, 50000, N, 33333, N, 45000], np.int32)
+    out, tr, plan, ctr = run_gpu(X, ke, K, family=family)
+    compare_rows(X, ke, K, out)
+    assert_counters_zero(ctr)
+    _, tr_ref = oracle_trace_for_plan(X, ke, K, plan)
+    compare_trace(tr, tr_ref)
+
+
+def test_worker_count_does_not_change_values():
+    M, N, K = 40, 66000, 2048
+    Xt, ket, K = workloads.generate("prefill_causal", M=M, N=N, K=K)
+    X, ke = Xt.numpy(), ket.numpy()
+    ref = oracle.topk_rows(X, ke, K)
+    traces = []
+    for w in (1, 7, 0):
+        out, tr, plan, ctr = run_gpu(X, ke, K, family=etk.FAMILY_PERSISTENT_SAMPLED, workers=w)
+        compare_rows(X, ke, K, out, ref=ref)
+        assert_counters_zero(ctr)
+        traces.append(tr)
+    assert all(np.array_equal(traces[0], t) for t in traces[1:])
+
+
+def test_default_entry_point_matches_plan_entry_point():
+    # exact_topk (default plan, PR-style API) vs the oracle, through the
+    # workspace_size / topk pair exactly as the pages' API describes.
+    M, N, K = 64, 65536, 2048
+    Xt, ket, K = workloads.generate("decode_batch", M=M, N=N, K=K)
+    dev = torch.device("cuda")
+    Xd, ked = Xt.to(dev), ket.to(dev)
+    cb, wb = etk.workspace_size(M, N, K)
+    counters = torch.zeros(cb, dtype=torch.uint8, device=dev)
+    workspace = torch.empty(wb, dtype=torch.uint8, device=dev)
+    out = torch.full((M, K), CANARY, dtype=torch.int32, device=dev)
+    nv = torch.tensor([M], dtype=torch.int32, device=dev)
+    for _ in range(3):
+        etk.topk(Xd, ked, out, nv, K, counters, workspace)
+    torch.cuda.synchronize()
+    compare_rows(Xt.numpy(), ket.numpy(), K, out.cpu().numpy())
+    assert_counters_zero(counters.cpu().numpy())
+
+
+def test_host_errors_launch_nothing():
+    dev = torch.device("cuda")
+    M, N, K = 4, 1000, 10
+    X = torch.randn(M, N, device=dev)
+    ke = torch.full((M,), N, dtype=torch.int32, device=dev)
+    out = torch.full((M, K), CANARY, dtype=torch.int32, device=dev)
+    cb, wb = etk.workspace_size(M, N, K)
+    counters = torch.zeros(cb, dtype=torch.uint8, device=dev)
+    ws = torch.empty(max(wb, 16), dtype=torch.uint8, device=dev)
+    lib = etk.library()
+    import ctypes
+    P = ctypes.c_void_p
+    stream = P(torch.cuda.current_stream().cuda_stream)
+    assert lib.exact_topk(None, M, N, P(ke.data_ptr()), P(out.data_ptr()), None, K,
+                          P(counters.data_ptr()), cb, P(ws.data_ptr()), wb, None, stream) == -1
+    assert lib.exact_topk(P(X.data_ptr()), M, N, P(ke.data_ptr()), P(out.data_ptr()), None, 0,
+                          P(counters.data_ptr()), cb, P(ws.data_ptr()), wb, None, stream) == -3
+    assert lib.exact_topk(P(X.data_ptr()), M, N, P(ke.data_ptr()), P(out.data_ptr()), None, K,
+                          P(counters.data_ptr()), cb - 16 if cb >= 16 else 0, P(ws.data_ptr()),
+                          wb, None, stream) == -4
+    assert lib.exact_topk(P(X.data_ptr() + 2), M, N, P(ke.data_ptr()), P(out.data_ptr()), None,
+                          K, P(counters.data_ptr()), cb, P(ws.data_ptr()), wb, None,
+                          stream) == -6
+    torch.cuda.synchronize()
+    assert (out.cpu().numpy() == CANARY).all()
