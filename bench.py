@@ -1,0 +1,556 @@
+"""Benchmark of exact row-wise FP32 Top-K on GB300.
+
+Metric: rows/s and score-row HBM GB/s (fraction of the measured GB300 HBM
+peak) per workload, 1 GPU.  The headline line is the decode batch (M=64,
+N=65536, ke ~ U[2048, 65536], K=2048, indexer-like scores); "per_config"
+repeats the measurement for all five workloads.
+
+A step is one exact Top-K call (one kernel launch) over one batch whose
+inputs are already resident in HBM.  Inputs smaller than L2 are rotated over
+copies whose total footprint is at least 4x the L2 size, so every call reads
+its scores from HBM.  Calls are captured in CUDA graphs and timed with CUDA
+events on the launching stream.
+
+Algorithmic bytes per call: sum_r clamp(ke[r], 0, N) * 4 (valid scores read
+once) + M * K * 4 (indices written).  Sampling, band and recovery rereads,
+frontier gathers and padding are not credited.
+
+``--impl reference`` times the CPU oracle (per-row std::nth_element, all host
+cores) on the same workload instead: the pages' own kernels are Hopper code
+that is not available here.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+HEADLINE = "decode_batch"
+MEASURED_PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+PROFILES = os.path.join(ROOT, "profiles")
+KERNEL_SOURCE = os.path.join(ROOT, "exact_top_selection_gb300", "csrc", "topk_kernels.cu")
+KERNEL_NAMES = {1: "persistent_sampled_kernel", 2: "kv_split_kernel", 3: "row_local_exact_kernel"}
+
+
+# ---------------------------------------------------------------- distributed helpers
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def aggregate_over_ranks(elapsed_s: float, rows: int, group=None):
+    """Whole-job numbers: the slowest rank's time and the rows of all ranks."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return elapsed_s, rows
+    dev = "cuda" if dist.get_backend(group) == "nccl" else "cpu"
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=dev)
+    n = torch.tensor([rows], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM, group=group)
+    return float(t.item()), int(n.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- peaks, profiles, clocks
+
+
+def hbm_peak():
+    try:
+        with open(MEASURED_PEAKS) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, earlier GB300 copy measurement)"
+
+
+def kernel_source_hash():
+    with open(KERNEL_SOURCE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, or None if there is
+    none or the kernel source changed since it was taken."""
+    path = os.path.join(PROFILES, f"{kernel}__{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    h = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    if not m or not h or h.group(1) != kernel_source_hash():
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the GPU is under load."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, interval_ms: int = 100):
+        self.gpu = gpu_index
+        self.interval = interval_ms
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", f"-lms={self.interval}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0=None, t1=None):
+        rows = [p for (t, p) in self.samples if (t0 is None or t >= t0) and (t1 is None or t <= t1)]
+        if not rows:
+            rows = [p for (_, p) in self.samples]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = sorted(v for v in (num(p[1]) for p in rows) if v is not None)
+        smax = max((v for v in (num(p[2]) for p in rows) if v is not None), default=None)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in rows for i in range(4) if p[5 + i] == "Active"})
+        power = [v for v in (num(p[3]) for p in rows) if v is not None]
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": smax,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------- workload setup
+
+
+def algorithmic_bytes(ke, N, M, K):
+    import torch
+    L = ke.to(torch.int64).clamp(0, N)
+    return int(L.sum().item()) * 4 + M * K * 4
+
+
+class Case:
+    """One workload resident on the device, rotated over enough copies to
+    defeat L2, with its runner (plan + counters + workspace)."""
+
+    def __init__(self, name, device, seed_offset=0, min_footprint_factor=4.0):
+        import torch
+
+        import exact_top_selection_gb300 as etk
+        import workloads
+
+        self.name = name
+        self.w = workloads.WORKLOADS[name]
+        self.device = device
+        X, ke, K = workloads.generate(name, device=str(device), seed=self.w.seed + seed_offset)
+        self.M, self.N = X.shape
+        self.K = K
+        self.ke = ke.to(device)
+        self.alg_bytes = algorithmic_bytes(self.ke, self.N, self.M, K)
+        l2 = torch.cuda.get_device_properties(device).L2_cache_size
+        per = X.numel() * 4
+        self.copies = max(1, math.ceil(min_footprint_factor * l2 / per)) if per < 2 * l2 else 1
+        self.X = [X] + [X.clone() for _ in range(self.copies - 1)]
+        self.runner = etk.ExactTopK(self.M, self.N, K, device=device)
+        self.plan = self.runner.plan
+        self.outs = [torch.empty(self.M, K, dtype=torch.int32, device=device)
+                     for _ in range(min(self.copies, 4))]
+        self.nv = torch.tensor([self.M], dtype=torch.int32, device=device)
+        self.l2_bytes = l2
+
+    def call(self, i, stream=None):
+        return self.runner(self.X[i % self.copies], self.ke, num_valid_rows=self.nv,
+                           out=self.outs[i % len(self.outs)], stream=stream)
+
+    def graph(self, n_calls, stream, start=0):
+        import torch
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            self.call(start, stream)  # first call on a device happens before capture
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for k in range(n_calls):
+                    self.call(start + k, stream)
+        return g
+
+    def l2_note(self):
+        if self.copies > 1:
+            return (f"inputs rotated over {self.copies} copies "
+                    f"({self.copies * self.X[0].numel() * 4 / self.l2_bytes:.1f}x L2)")
+        return "input larger than L2 (no rotation needed)"
+
+    def route_rates(self):
+        import torch
+
+        import exact_top_selection_gb300 as etk
+        tr = torch.full((self.M, 8), -9, dtype=torch.int32, device=self.device)
+        self.runner(self.X[0], self.ke, num_valid_rows=self.nv, out=self.outs[0], trace=tr)
+        torch.cuda.synchronize(self.device)
+        routes = tr[:, 0].cpu().tolist()
+        counts = {}
+        for r in routes:
+            counts[etk.ROUTES[r] if 0 <= r < len(etk.ROUTES) else str(r)] = \
+                counts.get(etk.ROUTES[r] if 0 <= r < len(etk.ROUTES) else str(r), 0) + 1
+        long_rows = sum(v for k, v in counts.items() if k != "pad")
+        band = counts.get("band", 0) + counts.get("exact_after_band", 0)
+        exact = sum(counts.get(k, 0) for k in ("exact_after_band", "exact_no_band",
+                                               "direct_exact", "guess_exact"))
+        return {"counts": counts,
+                "p_band": band / long_rows if long_rows else 0.0,
+                "p_exact": exact / long_rows if long_rows else 0.0}
+
+
+def time_schedule(case, steps, warmup, stream, max_nodes=512):
+    """Runs `warmup` untimed calls, then times exactly `steps` calls (CUDA graph
+    replays on `stream`, CUDA events on the same stream).  Returns seconds."""
+    import torch
+    G = max(1, min(max_nodes, steps, max(case.copies, 64)))
+    full = case.graph(G, stream)
+    rem = steps % G
+    tail = case.graph(rem, stream) if rem else None
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            case.call(i, stream)
+    torch.cuda.synchronize(case.device)
+    barrier()
+    torch.cuda.synchronize(case.device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps // G):
+            full.replay()
+        if tail is not None:
+            tail.replay()
+        e1.record(stream)
+    torch.cuda.synchronize(case.device)
+    barrier()
+    torch.cuda.synchronize(case.device)
+    return e0.elapsed_time(e1) / 1e3
+
+
+def median_per_call(case, stream, rounds=7, calls_per_round=None):
+    """Paper-style protocol: conditioning sweeps, then rounds of graph replays;
+    median over rounds of the mean per-call time (seconds)."""
+    import torch
+    n = calls_per_round or max(100, case.copies)
+    n = min(n, 1024)
+    g = case.graph(n, stream)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize(case.device)
+    times = []
+    for _ in range(rounds):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(case.device)
+        times.append(e0.elapsed_time(e1) / 1e3 / n)
+    times.sort()
+    return times[len(times) // 2]
+
+
+def keep_busy(case, stream, seconds):
+    """Untimed replays so that clock samples exist for short timed regions."""
+    import torch
+    g = case.graph(min(256, max(case.copies, 16)), stream)
+    t_end = time.time() + seconds
+    while time.time() < t_end:
+        g.replay()
+        torch.cuda.synchronize(case.device)
+
+
+def e2e_measure(case, steps, warmup, stream):
+    """Same metric through the public API with host buffers: per step, H2D of
+    the score matrix, lengths and live count from pinned memory, the call, and
+    D2H of the indices, all inside the timed region."""
+    import torch
+    Xh = case.X[0].cpu().pin_memory()
+    keh = case.ke.cpu().pin_memory()
+    nvh = case.nv.cpu().pin_memory()
+    outh = torch.empty(case.M, case.K, dtype=torch.int32).pin_memory()
+    Xd = torch.empty_like(case.X[0])
+    ked = torch.empty_like(case.ke)
+    nvd = torch.empty_like(case.nv)
+    outd = torch.empty(case.M, case.K, dtype=torch.int32, device=case.device)
+
+    def step():
+        Xd.copy_(Xh, non_blocking=True)
+        ked.copy_(keh, non_blocking=True)
+        nvd.copy_(nvh, non_blocking=True)
+        case.runner(Xd, ked, num_valid_rows=nvd, out=outd, stream=stream)
+        outh.copy_(outd, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(warmup, 3)):
+            step()
+        torch.cuda.synchronize(case.device)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+    torch.cuda.synchronize(case.device)
+    dt = e0.elapsed_time(e1) / 1e3
+    h2d = Xh.numel() * 4 + keh.numel() * 4 + nvh.numel() * 4
+    d2h = outh.numel() * 4
+    return dt, h2d, d2h
+
+
+def cpu_baseline(case_name, seconds=10.0, rows_cap=None):
+    """The oracle as it stands, on all host cores, over a bounded sample."""
+    import numpy as np
+
+    import oracle
+    import workloads
+    X, ke, K = workloads.generate(case_name, device="cpu")
+    X, ke = X.numpy(), ke.numpy()
+    M = X.shape[0] if rows_cap is None else min(rows_cap, X.shape[0])
+    threads = oracle.hardware_threads()
+    rows = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.topk_rows(X[:M], ke[:M], K, nthreads=threads)
+        rows += M
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    bytes_ = int(np.clip(ke[:M].astype(np.int64), 0, X.shape[1]).sum()) * 4 + M * K * 4
+    return {"value": rows / dt, "unit": "rows/s", "cores": threads, "kind": "oracle",
+            "gbs": bytes_ * (rows / M) / dt / 1e9,
+            "sample": f"{case_name}: {M} of {X.shape[0]} rows per pass, {rows // M} passes "
+                      f"in {dt:.1f} s (std::nth_element per row, {threads} threads)"}
+
+
+# ---------------------------------------------------------------- arms
+
+
+def run_ours(args):
+    import torch
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local_rank if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(device)
+    stream = torch.cuda.Stream(device)
+    peak, peak_src = hbm_peak()
+
+    case = Case(args.workload, device, seed_offset=rank)
+    sampler = ClockSampler(device.index).start()
+    time.sleep(0.3)
+    t_load0 = time.time()
+    elapsed = time_schedule(case, args.steps, args.warmup, stream)
+    if elapsed < 1.0:
+        keep_busy(case, stream, 1.0 - elapsed)
+    t_load1 = time.time()
+    clocks = sampler.summary(t_load0, t_load1)
+    e_max, rows_total = aggregate_over_ranks(elapsed, case.M * args.steps)
+    value = rows_total / e_max
+    per_call = elapsed / args.steps
+    achieved = case.alg_bytes / per_call / 1e9
+    kernel = KERNEL_NAMES[case.plan.family]
+    traffic = profiled_traffic(kernel, case.name)
+
+    e2e = None
+    if not args.no_e2e:
+        dt, h2d, d2h = e2e_measure(case, max(3, min(args.steps, 200)), args.warmup, stream)
+        n_e2e = max(3, min(args.steps, 200))
+        e_dt, e_rows = aggregate_over_ranks(dt, case.M * n_e2e)
+        e2e = {"value": e_rows / e_dt, "unit": "rows/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": dt / n_e2e * 1e3,
+               "path": "pinned host -> H2D -> exact_topk_run (C ABI) -> D2H, per step"}
+
+    per_config = {}
+    if args.all_configs:
+        import workloads
+        for name in workloads.ORDER:
+            c = case if name == case.name else Case(name, device, seed_offset=rank)
+            sec = median_per_call(c, stream)
+            gbs = c.alg_bytes / sec / 1e9
+            per_config[name] = {
+                "workload": c.w.description, "M": c.M, "N": c.N, "K": c.K,
+                "family": KERNEL_NAMES[c.plan.family], "stride": c.plan.stride,
+                "dual": c.plan.dual, "splits": c.plan.splits, "workers": c.plan.workers,
+                "us_per_call": sec * 1e6, "rows_per_s": c.M / sec, "gbs": gbs,
+                "frac_of_hbm_peak": gbs / peak, "alg_bytes_per_call": c.alg_bytes,
+                "l2": c.l2_note(), "routes": c.route_rates(),
+                "traffic_bytes_per_launch": profiled_traffic(KERNEL_NAMES[c.plan.family], name),
+            }
+            if c is not case:
+                del c
+                torch.cuda.empty_cache()
+    sampler.stop()
+    clocks_all = sampler.summary()
+
+    cpu = None
+    if world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(case.name, seconds=args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": "rows/s and score-row HBM GB/s (fraction of GB300 peak) per config, 1 GPU",
+            "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": e_max / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded; indexer-like scores stand in for the paper's captures)",
+            "config": {"workload": case.w.description, "name": case.name, "M": case.M,
+                       "N": case.N, "K": case.K, "l2": case.l2_note(),
+                       "family": KERNEL_NAMES[case.plan.family], "stride": case.plan.stride,
+                       "dual": case.plan.dual, "splits": case.plan.splits,
+                       "parallelism": f"replicas x{world} (rows are independent)"},
+            "score_row_gbs": achieved,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic, "kernel": kernel,
+                         "peak_source": peak_src,
+                         "alg_bytes_per_launch": case.alg_bytes},
+            "gpu_launches": args.steps,
+            "clocks": {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+            "clock_samples": clocks.get("samples"),
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "per_config": per_config,
+            "clocks_whole_run": clocks_all,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle, timed on the host's cores, on the
+    same workload, each step a bounded sample of its rows."""
+    import numpy as np
+
+    import oracle
+    import workloads
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    X, ke, K = workloads.generate(args.workload, device="cpu")
+    X, ke = X.numpy(), ke.numpy()
+    M, N = X.shape
+    threads = oracle.hardware_threads()
+    t0 = time.perf_counter()
+    oracle.topk_rows(X[:min(M, 8)], ke[:min(M, 8)], K, nthreads=threads)
+    per_row = (time.perf_counter() - t0) / min(M, 8)
+    budget = args.reference_seconds / max(1, args.steps + args.warmup)
+    rows_per_step = int(max(1, min(M, budget / max(per_row, 1e-9))))
+    for i in range(args.warmup):
+        oracle.topk_rows(X[:rows_per_step], ke[:rows_per_step], K, nthreads=threads)
+    t0 = time.perf_counter()
+    done = 0
+    for i in range(args.steps):
+        lo = (i * rows_per_step) % M
+        hi = min(M, lo + rows_per_step)
+        oracle.topk_rows(X[lo:hi], ke[lo:hi], K, nthreads=threads)
+        done += hi - lo
+    dt = time.perf_counter() - t0
+    value = done / dt
+    w = workloads.WORKLOADS[args.workload]
+    cpu = {"value": value, "unit": "rows/s", "cores": threads, "kind": "oracle",
+           "sample": f"{rows_per_step} of {M} rows per step"}
+    line = {"impl": "reference",
+            "metric": "rows/s and score-row HBM GB/s (fraction of GB300 peak) per config, 1 GPU",
+            "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt / max(1, args.steps) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": {"workload": w.description, "name": w.name, "M": M,
+                                            "N": N, "K": K},
+            "cpu_baseline": cpu,
+            "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--all-configs", dest="all_configs", action="store_true", default=True)
+    ap.add_argument("--headline-only", dest="all_configs", action="store_false")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--reference-seconds", type=float, default=60.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.steps < 1:
+        ap.error("--steps must be >= 1")
+    return args
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        import __graft_entry__
+        __graft_entry__.build()
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

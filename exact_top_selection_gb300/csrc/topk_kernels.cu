@@ -1006,14 +1006,24 @@ __global__ void __launch_bounds__(kKvSplitThreads, 3) kv_split_kernel(Params p) 
   write_trace(p, r, route, tau0, guess ? -1 : tau1, (int)c0, c1, tstar, e0, q0n);
 }
 
+// Kernel attributes are set once per (device, kernel); later launches, which
+// may be inside a stream capture, only launch.
+constexpr int kMaxDevices = 64;
+volatile int g_attr_smem[kMaxDevices][4];
+
 template <class KernelT>
-int set_attrs(KernelT kernel, size_t smem) {
+int set_attrs(KernelT kernel, int family, size_t smem) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return EXACT_TOPK_ERR_CUDA;
+  const bool cached = dev >= 0 && dev < kMaxDevices;
+  if (cached && g_attr_smem[dev][family] >= (int)smem) return EXACT_TOPK_OK;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return EXACT_TOPK_ERR_CUDA;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared) != cudaSuccess)
     return EXACT_TOPK_ERR_CUDA;
+  if (cached) g_attr_smem[dev][family] = (int)smem;
   return EXACT_TOPK_OK;
 }
 
@@ -1032,18 +1042,18 @@ int kernel_occupancy(int family, int device, int* ctas_per_sm) {
   cudaError_t e = cudaSuccess;
   if (family == EXACT_TOPK_FAMILY_PERSISTENT_SAMPLED) {
     const size_t smem = shared_bytes(family, kPersistentCap);
-    rc = set_attrs(persistent_sampled_kernel, smem);
+    rc = set_attrs(persistent_sampled_kernel, EXACT_TOPK_FAMILY_PERSISTENT_SAMPLED, smem);
     if (rc == EXACT_TOPK_OK)
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, persistent_sampled_kernel,
                                                         kPersistentThreads, smem);
   } else if (family == EXACT_TOPK_FAMILY_KV_SPLIT) {
     const size_t smem = shared_bytes(family, kKvSplitCap);
-    rc = set_attrs(kv_split_kernel, smem);
+    rc = set_attrs(kv_split_kernel, EXACT_TOPK_FAMILY_KV_SPLIT, smem);
     if (rc == EXACT_TOPK_OK)
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kv_split_kernel, kKvSplitThreads, smem);
   } else {
     const size_t smem = shared_bytes(family, kRowLocalCap);
-    rc = set_attrs(row_local_exact_kernel, smem);
+    rc = set_attrs(row_local_exact_kernel, EXACT_TOPK_FAMILY_ROW_LOCAL_EXACT, smem);
     if (rc == EXACT_TOPK_OK)
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, row_local_exact_kernel,
                                                         kRowLocalThreads, smem);
@@ -1093,19 +1103,19 @@ int launch(const exact_topk_plan& plan, const LaunchArgs& a, cudaStream_t stream
   int rc = EXACT_TOPK_OK;
   switch (plan.family) {
     case EXACT_TOPK_FAMILY_PERSISTENT_SAMPLED:
-      rc = set_attrs(persistent_sampled_kernel, smem);
+      rc = set_attrs(persistent_sampled_kernel, EXACT_TOPK_FAMILY_PERSISTENT_SAMPLED, smem);
       if (rc != EXACT_TOPK_OK) return rc;
       persistent_sampled_kernel<<<plan.workers, kPersistentThreads, smem, stream>>>(p);
       break;
     case EXACT_TOPK_FAMILY_KV_SPLIT: {
-      rc = set_attrs(kv_split_kernel, smem);
+      rc = set_attrs(kv_split_kernel, EXACT_TOPK_FAMILY_KV_SPLIT, smem);
       if (rc != EXACT_TOPK_OK) return rc;
       const dim3 grid((unsigned)plan.splits, (unsigned)plan.num_rows);
       kv_split_kernel<<<grid, kKvSplitThreads, smem, stream>>>(p);
       break;
     }
     case EXACT_TOPK_FAMILY_ROW_LOCAL_EXACT:
-      rc = set_attrs(row_local_exact_kernel, smem);
+      rc = set_attrs(row_local_exact_kernel, EXACT_TOPK_FAMILY_ROW_LOCAL_EXACT, smem);
       if (rc != EXACT_TOPK_OK) return rc;
       row_local_exact_kernel<<<plan.workers, kRowLocalThreads, smem, stream>>>(p);
       break;
