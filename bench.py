@@ -184,7 +184,7 @@ class Case:
     """One workload resident on the device, rotated over enough copies to
     defeat L2, with its runner (plan + counters + workspace)."""
 
-    def __init__(self, name, device, seed_offset=0, min_footprint_factor=4.0):
+    def __init__(self, name, device, seed_offset=0, min_footprint_factor=4.0, rows=None):
         import torch
 
         import exact_top_selection_gb300 as etk
@@ -193,7 +193,8 @@ class Case:
         self.name = name
         self.w = workloads.WORKLOADS[name]
         self.device = device
-        X, ke, K = workloads.generate(name, device=str(device), seed=self.w.seed + seed_offset)
+        X, ke, K = workloads.generate(name, M=rows, device=str(device),
+                                      seed=self.w.seed + seed_offset)
         self.M, self.N = X.shape
         self.K = K
         self.ke = ke.to(device)
@@ -393,7 +394,7 @@ def run_ours(args):
     stream = torch.cuda.Stream(device)
     peak, peak_src = hbm_peak()
 
-    case = Case(args.workload, device, seed_offset=rank)
+    case = Case(args.workload, device, seed_offset=rank, rows=args.rows)
     sampler = ClockSampler(device.index).start()
     time.sleep(0.3)
     t_load0 = time.time()
@@ -422,7 +423,8 @@ def run_ours(args):
     if args.all_configs:
         import workloads
         for name in workloads.ORDER:
-            c = case if name == case.name else Case(name, device, seed_offset=rank)
+            c = case if (name == case.name and args.rows is None) else \
+                Case(name, device, seed_offset=rank)
             sec = median_per_call(c, stream)
             gbs = c.alg_bytes / sec / 1e9
             per_config[name] = {
@@ -528,6 +530,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--rows", type=int, default=None,
+                    help="row count override (smaller cases for profiling)")
     ap.add_argument("--all-configs", dest="all_configs", action="store_true", default=True)
     ap.add_argument("--headline-only", dest="all_configs", action="store_false")
     ap.add_argument("--no-e2e", action="store_true")
