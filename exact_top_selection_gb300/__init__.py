@@ -40,7 +40,7 @@ TRACE_FIELDS = ("route", "tau0", "tau1", "c0", "c1", "tau_star", "e0", "q0")
 
 EXPORTED_SYMBOLS = ("exact_topk_query_device", "exact_topk_make_plan", "exact_topk_workspace_size",
                     "exact_topk", "exact_topk_run", "exact_topk_error_string",
-                    "exact_topk_version")
+                    "exact_topk_version", "exact_topk_kv_split_noalloc")
 
 
 class ExactTopKError(RuntimeError):
@@ -111,6 +111,8 @@ def library():
     lib.exact_topk_error_string.argtypes = [c_int]
     lib.exact_topk_error_string.restype = ctypes.c_char_p
     lib.exact_topk_version.argtypes = []
+    lib.exact_topk_kv_split_noalloc.argtypes = [p, c_i64, c_i64, p, p, p, c_int, p]
+    lib.exact_topk_kv_split_noalloc.restype = c_int
     for name in ("exact_topk_query_device", "exact_topk_make_plan", "exact_topk_workspace_size",
                  "exact_topk", "exact_topk_run", "exact_topk_version"):
         getattr(lib, name).restype = c_int

@@ -29,6 +29,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "etk_internal.h"
 
@@ -1126,3 +1127,86 @@ int launch(const exact_topk_plan& plan, const LaunchArgs& a, cudaStream_t stream
 }
 
 }  // namespace etk
+
+// ----------------------------------------------------------------------------
+// Allocation-free entry point
+// ----------------------------------------------------------------------------
+//
+// Some callers cannot allocate device memory at the point where they need a
+// Top-K: code that runs while a stream capture is already open (a cudaMalloc
+// there would invalidate the capture), plugins whose host framework owns every
+// device allocation, and latency-critical loops where cudaMalloc's implicit
+// device synchronization is unacceptable.  For them this entry point runs the
+// KV-split kernel with its counters and workspace carved out of one file-scope
+// device array instead of caller-provided buffers.
+
+namespace etk {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;  // EXACT_TOPK_NOALLOC_SCRATCH_BYTES
+
+// Loaded with the library's device code on every GPU that uses the library and
+// kept until the process exits.  Shared by every call on that device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices];
+bool g_noalloc_have_info[kMaxDevices];
+exact_topk_device_info g_noalloc_info[kMaxDevices];
+
+// Once per device, with that device current: the device address of the
+// scratch array (the host-side symbol is only a stand-in, never a device
+// pointer) and the device facts the planner needs.
+int noalloc_setup(int dev, void** ptr, exact_topk_device_info* info) {
+  if (dev < 0 || dev >= kMaxDevices) return EXACT_TOPK_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return EXACT_TOPK_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  if (!g_noalloc_have_info[dev]) {
+    const int rc = exact_topk_query_device(dev, &g_noalloc_info[dev]);
+    if (rc != EXACT_TOPK_OK) return rc;
+    g_noalloc_have_info[dev] = true;
+  }
+  *ptr = g_noalloc_ptr[dev];
+  *info = g_noalloc_info[dev];
+  return EXACT_TOPK_OK;
+}
+
+}  // namespace
+}  // namespace etk
+
+extern "C" int exact_topk_kv_split_noalloc(const float* logits, int64_t num_rows,
+                                           int64_t max_kv_len, const int32_t* ke, int32_t* out,
+                                           const int32_t* num_valid_rows, int top_k,
+                                           struct CUstream_st* stream) {
+  using namespace etk;
+  if (logits == nullptr || ke == nullptr || out == nullptr) return EXACT_TOPK_ERR_NULL_POINTER;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return EXACT_TOPK_ERR_CUDA;
+  void* base = nullptr;
+  exact_topk_device_info info;
+  int rc = noalloc_setup(dev, &base, &info);
+  if (rc != EXACT_TOPK_OK) return rc;
+  exact_topk_plan_request req{};
+  req.family = EXACT_TOPK_FAMILY_KV_SPLIT;
+  req.dual = -1;
+  exact_topk_plan plan;
+  rc = exact_topk_make_plan(num_rows, max_kv_len, max_kv_len, top_k, &info, &req, &plan);
+  if (rc != EXACT_TOPK_OK) return rc;
+  const uint64_t ctr_bytes = (plan.counter_bytes + 255u) / 256u * 256u;
+  if (ctr_bytes + plan.workspace_bytes > kNoAllocScratchBytes)
+    return EXACT_TOPK_ERR_WORKSPACE_TOO_SMALL;
+  unsigned char* scratch = static_cast<unsigned char*>(base);
+  // The array keeps whatever the previous call left; the counters must start
+  // at zero, so clear them on the stream (a memset, not an allocation).
+  if (cudaMemsetAsync(scratch, 0, (size_t)plan.counter_bytes,
+                      reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return EXACT_TOPK_ERR_CUDA;
+  return exact_topk_run(&plan, logits, ke, out, num_valid_rows, scratch,
+                        (size_t)plan.counter_bytes, scratch + ctr_bytes,
+                        (size_t)plan.workspace_bytes, nullptr, nullptr, stream);
+}

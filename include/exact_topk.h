@@ -193,6 +193,35 @@ int exact_topk_run(const exact_topk_plan* plan, const float* logits, const int32
                    size_t counter_bytes, void* workspace, size_t workspace_bytes,
                    const int32_t* prev_topk, int32_t* trace, struct CUstream_st* stream);
 
+/* Allocation-free variant of exact_topk for callers that cannot allocate
+ * device memory where they need the selection: code running while a stream
+ * capture is already open (a cudaMalloc there would invalidate the capture),
+ * plugins whose host framework owns every device allocation, and
+ * latency-critical loops where cudaMalloc's implicit device synchronization is
+ * not acceptable.  The paper has no counterpart to this entry point.
+ *
+ * It always runs the KV-split kernel family (planned as for exact_topk with
+ * the family fixed) and takes its counters and workspace from one static
+ * device array of EXACT_TOPK_NOALLOC_SCRATCH_BYTES that every GPU using the
+ * library holds until the process exits.  The caller still passes the scores,
+ * lengths, live-row count and output, with the meaning, layout and alignment
+ * rules of exact_topk; there is no guess source.
+ *   - Shapes whose KV-split counters (rounded up to 256 bytes) plus workspace
+ *     (about num_rows * max_kv_len * 8 bytes) exceed the array are rejected
+ *     with EXACT_TOPK_ERR_WORKSPACE_TOO_SMALL; nothing is launched.
+ *   - The first call on a device sets up (the array's device address, device
+ *     attributes, kernel attributes): make it before any stream capture.
+ *   - Each call enqueues a memset of the counter region and one kernel on
+ *     `stream`; it calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - Every call on a device shares the one array, which keeps the previous
+ *     call's contents: calls that overlap on the GPU (other streams, other
+ *     host threads) race and must be serialized by the caller.
+ * Errors: as exact_topk. */
+#define EXACT_TOPK_NOALLOC_SCRATCH_BYTES (64u << 20)
+int exact_topk_kv_split_noalloc(const float* logits, int64_t num_rows, int64_t max_kv_len,
+                                const int32_t* ke, int32_t* out, const int32_t* num_valid_rows,
+                                int top_k, struct CUstream_st* stream);
+
 /* Static description of a status code; never NULL. */
 const char* exact_topk_error_string(int status);
 
