@@ -46,8 +46,7 @@ size_t shared_bytes(int family, int cap);
 
 // Workspace carve-up shared by the planner and the launcher.
 struct WorkspaceLayout {
-  uint64_t idx_offset;    // int32 [slices][N]
-  uint64_t key_offset;    // uint32 [slices][N]
+  uint64_t pair_offset;   // (int32 index, uint32 key) pairs [slices][N]
   uint64_t seg_offset;    // int32 pairs [M][P] (KV-split published counts)
   uint64_t total;
   int64_t slices;

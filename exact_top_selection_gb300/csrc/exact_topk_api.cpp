@@ -69,10 +69,8 @@ WorkspaceLayout workspace_layout(const exact_topk_plan& plan) {
   }
   uint64_t off = 0;
   lay.slices = slices;
-  lay.idx_offset = off;
-  off = round_up(off + (uint64_t)slices * (uint64_t)N * 4u, kAlign);
-  lay.key_offset = off;
-  off = round_up(off + (uint64_t)slices * (uint64_t)N * 4u, kAlign);
+  lay.pair_offset = off;
+  off = round_up(off + (uint64_t)slices * (uint64_t)N * 8u, kAlign);
   lay.seg_offset = off;
   if (plan.family == EXACT_TOPK_FAMILY_KV_SPLIT)
     off = round_up(off + (uint64_t)plan.num_rows * (uint64_t)plan.splits * 8u, kAlign);
@@ -218,7 +216,7 @@ int exact_topk_make_plan(int64_t num_rows, int64_t max_kv_len, int64_t row_pitch
       while (P < 64 && num_rows * P < target) P *= 2;
       while (P > 1 && max_kv_len / P < 8192) P /= 2;
     }
-    if (P < 1 || P > 256 || num_rows > 65535) return EXACT_TOPK_ERR_BAD_PLAN;
+    if (P < 1 || P > 128 || num_rows > 65535) return EXACT_TOPK_ERR_BAD_PLAN;
     p.splits = (int32_t)P;
     p.workers = (int32_t)(num_rows * P);
   } else {
@@ -269,7 +267,7 @@ int exact_topk_run(const exact_topk_plan* plan, const float* logits, const int32
       plan->q1 < 1 || (plan->dual != 0 && plan->dual != 1))
     return EXACT_TOPK_ERR_BAD_PLAN;
   if (plan->family == EXACT_TOPK_FAMILY_KV_SPLIT &&
-      (plan->num_rows > 65535 || plan->splits > 256 ||
+      (plan->num_rows > 65535 || plan->splits > 128 ||
        (int64_t)plan->workers != plan->num_rows * plan->splits))
     return EXACT_TOPK_ERR_BAD_PLAN;
   const int expect_cap = plan->family == EXACT_TOPK_FAMILY_PERSISTENT_SAMPLED

@@ -24,6 +24,12 @@
 // projection.  NaN is outside the contract; to keep c monotone along the full
 // key space (and so every count consistent) positive NaNs are placed in bin 0
 // and negative NaNs in bin 2047, matching their key order.
+//
+// Complete-row passes stream the row with 256-bit loads that carry an L2
+// evict-first hint, so the lines the Phase-1 view touched (loaded with normal
+// priority) tend to stay in L2 until the complete-row pass reaches them.  Each
+// thread filters a tile of 16 scores with one max (or min) reduction; only
+// tiles holding a candidate take the warp-aggregated append path.
 
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -37,6 +43,21 @@ namespace etk {
 namespace {
 
 constexpr int kCoarseBins = 2048;
+constexpr int kMaxSplits = 128;
+// Resident CTAs per SM the sampled kernels are compiled for (register budget).
+#ifndef ETK_SAMPLED_MIN_CTAS
+#define ETK_SAMPLED_MIN_CTAS 2
+#endif
+// 256-bit loads per thread per tile of a complete-row pass.
+#ifndef ETK_TILE_V8
+#define ETK_TILE_V8 2
+#endif
+// L2 eviction hint of complete-row loads: 1 = evict first, 0 = none.
+#ifndef ETK_L2_EVICT_FIRST
+#define ETK_L2_EVICT_FIRST 1
+#endif
+constexpr int kTileV8 = ETK_TILE_V8;
+constexpr int kTileScores = 8 * kTileV8;
 constexpr uint32_t kDescPosInf = 0x007FFFFFu;  // kappa_down32(+inf)
 constexpr uint32_t kDescNegInf = 0xFF800000u;  // kappa_down32(-inf)
 constexpr unsigned kFull = 0xFFFFFFFFu;
@@ -62,19 +83,33 @@ __device__ __forceinline__ int coarse_bin(uint32_t u, uint32_t d) {
   return (int)(d16 >> 5);
 }
 
+__device__ __forceinline__ int coarse_bin(uint32_t u) { return coarse_bin(u, desc_key(u)); }
+
 // Largest kappa_down32 key whose coarse bin is <= tau: the inclusive FP32
 // endpoint of the admitted prefix (section 4.3; section 5.2 "converts the
 // selected bins to their inclusive FP32 endpoints").  c is non-decreasing along
-// the key space, so a binary search finds it.
-__device__ uint32_t cutoff_for_bin(int tau) {
-  uint32_t lo = 0u, hi = 0xFFFFFFFFu;  // c(key 0) = 0 <= tau for tau >= 0
+// the key space, so a search finds it; the 32 lanes of one warp test 32
+// evenly spaced keys per step, shrinking the interval ~33-fold.  Must be
+// called by all 32 lanes of a warp; every lane returns the result.
+__device__ uint32_t cutoff_for_bin_warp(int tau) {
+  const int lane = threadIdx.x & 31;
+  uint32_t lo = 0u, hi = 0xFFFFFFFFu;  // c(lo) <= tau for tau >= 0; answer in [lo, hi]
   while (lo < hi) {
-    const uint32_t mid = lo + (uint32_t)((((uint64_t)(hi - lo)) + 1ull) >> 1);
-    const uint32_t u = bits_from_desc(mid);
-    if (coarse_bin(u, mid) <= tau)
-      lo = mid;
-    else
-      hi = mid - 1u;
+    const uint32_t n = hi - lo;
+    // 32 test points lo + (l + 1) * step, clamped to hi: non-decreasing in l.
+    const uint32_t step = n <= 32u ? 1u : (uint32_t)(((uint64_t)n + 31u) >> 5);
+    const uint64_t pp = (uint64_t)lo + (uint64_t)(lane + 1) * step;
+    const uint32_t p = pp > hi ? hi : (uint32_t)pp;
+    const bool ok = coarse_bin(bits_from_desc(p), p) <= tau;
+    const unsigned m = __ballot_sync(kFull, ok);
+    const int k = __popc(m);  // passing lanes form a prefix
+    if (k == 0) {
+      hi = __shfl_sync(kFull, p, 0) - 1u;
+    } else {
+      const uint32_t pk = __shfl_sync(kFull, p, k & 31);
+      lo = __shfl_sync(kFull, p, k - 1);
+      if (k < 32) hi = pk - 1u;
+    }
   }
   return lo;
 }
@@ -88,13 +123,20 @@ __device__ __forceinline__ uint32_t digit(uint32_t d, int j) {
 // Loads
 // ----------------------------------------------------------------------------
 
-// Streaming 128-bit load of score bits that are read once per pass.
-__device__ __forceinline__ uint4 ld_stream4(const uint4* p) {
-  uint4 v;
-  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+// 256-bit streaming load of 8 score bit patterns (32-byte aligned address),
+// read once per complete-row pass: no L1 allocation, evict first from L2.
+__device__ __forceinline__ void ld_stream8(const float* p, uint32_t* x) {
+#if ETK_L2_EVICT_FIRST
+  asm("ld.global.nc.L1::no_allocate.L2::evict_first.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]), "=r"(x[4]), "=r"(x[5]), "=r"(x[6]),
+        "=r"(x[7])
       : "l"(p));
-  return v;
+#else
+  asm("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]), "=r"(x[4]), "=r"(x[5]), "=r"(x[6]),
+        "=r"(x[7])
+      : "l"(p));
+#endif
 }
 
 __device__ __forceinline__ uint32_t ld_stream1(const float* p) {
@@ -108,14 +150,19 @@ __device__ __forceinline__ uint32_t ld_stream1(const float* p) {
 // ----------------------------------------------------------------------------
 
 struct alignas(16) RowState {
-  uint32_t hist[kCoarseBins];  // one allocation: h_{r,s} -> h0 -> h1 -> h2 (Fig. 5)
+  uint32_t hist[kCoarseBins];   // h_{r,s} -> h0 (Fig. 5); refinement alternates with hist2
+  uint32_t hist2[kCoarseBins];
   uint32_t warp_sums[32];
+  uint32_t run_pre[kMaxSplits + 1];  // KV-split finisher: run prefix over segments
+  uint32_t run_c0[kMaxSplits];       // KV-split finisher: primary count per segment
+  uint32_t run_cb[kMaxSplits];       // KV-split finisher: band count per segment
   int32_t res_bin[2];
   uint32_t res_below[2];
   uint32_t res_cnt[2];
   uint32_t n_front;  // frontier entries
   uint32_t n_out;    // output slots used
   uint32_t n_keep;   // survivors during an in-place compaction
+  uint32_t n_drop;   // sink for counts that are not kept
   uint32_t cut[2];   // kappa_down32 cutoffs
   int32_t gmax;      // guess source: worst coarse bin
   int32_t ginvalid;  // guess source: an entry outside [0, L)
@@ -123,8 +170,8 @@ struct alignas(16) RowState {
   int32_t is_last;
   uint32_t seg_c0;   // KV-split: this segment's primary candidates
   uint32_t seg_cb;   // KV-split: this segment's band candidates
-  uint32_t total;    // KV-split finisher: merged count
-  int32_t pad_[1];
+  uint32_t tot_c0;   // KV-split finisher: merged counts
+  uint32_t tot_cb;
 };
 
 struct Params {
@@ -144,8 +191,7 @@ struct Params {
   int32_t* out;
   const int32_t* num_valid_rows;
   int32_t* counters;
-  int32_t* ws_idx;   // [slices][N]
-  uint32_t* ws_key;  // [slices][N]
+  uint2* ws;            // [slices][N] (index, key) pairs
   int32_t* seg_counts;  // [M_cap][P][2]
   const int32_t* prev;
   int32_t* trace;
@@ -155,36 +201,36 @@ struct Params {
 // at logical positions >= cap live at the same position of a global slice of
 // capacity gcap (section 5.4: "Two global ping-pong slices extend the shared
 // frontier"; here one slice suffices because compaction is done in place).
+// Entries are (index, key) pairs stored together.
 struct Frontier {
-  int32_t* s_idx;
-  uint32_t* s_key;
+  uint2* s;
   uint32_t cap;
-  int32_t* g_idx;
-  uint32_t* g_key;
+  uint2* g;
   uint32_t gcap;
 
   __device__ __forceinline__ void put(uint32_t p, int32_t i, uint32_t d) const {
-    if (p < cap) {
-      s_idx[p] = i;
-      s_key[p] = d;
-    } else if (p < gcap) {
-      g_idx[p] = i;
-      g_key[p] = d;
-    }
+    if (p < cap)
+      s[p] = make_uint2((uint32_t)i, d);
+    else if (p < gcap)
+      g[p] = make_uint2((uint32_t)i, d);
   }
   __device__ __forceinline__ void get(uint32_t p, int32_t& i, uint32_t& d) const {
-    if (p < cap) {
-      i = s_idx[p];
-      d = s_key[p];
-    } else if (p < gcap) {
-      i = __ldcg(g_idx + p);
-      d = __ldcg(g_key + p);
-    } else {
-      i = -1;
-      d = 0xFFFFFFFFu;
-    }
+    uint2 e = make_uint2(0xFFFFFFFFu, 0xFFFFFFFFu);
+    if (p < cap)
+      e = s[p];
+    else if (p < gcap)
+      e = __ldcg(g + p);
+    i = (int32_t)e.x;
+    d = e.y;
   }
 };
+
+// Dynamic shared memory: RowState, then cap frontier pairs, then one
+// candidate-vector stack per warp.
+__device__ __forceinline__ uint32_t* queue_area(const Params& p) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  return reinterpret_cast<uint32_t*>(smem_raw + sizeof(RowState) + sizeof(uint2) * (size_t)p.cap);
+}
 
 __device__ __forceinline__ void flag_status(int32_t* counters, int bit) {
   atomicOr(counters + kCtrStatus, bit);
@@ -195,45 +241,42 @@ __device__ __forceinline__ void clear_hist(RowState& st, int nbins) {
   for (int b = threadIdx.x; b < nbins; b += THREADS) st.hist[b] = 0u;
 }
 
-// For each target t of `targets` (ntargets <= 2): res_bin = min{b : H(b) >= t}
-// over the inclusive prefix H of hist[0, nbins), res_below = H(b - 1) and
-// res_cnt = hist[b]; res_bin = -1 when the total is below t.  The histogram is
-// only read.  Must be entered by the whole CTA after the histogram is complete;
-// results are visible to every thread on return.
+// For each target t (ntargets <= 2): res_bin = min{b : H(b) >= t} over the
+// inclusive prefix H of hist[0, nbins), res_below = H(b - 1) and res_cnt =
+// hist[b]; res_bin = -1 (res_below = total) when the total is below t.  The
+// histogram is only read.  Must be entered by the whole CTA after the
+// histogram is complete, with a barrier between consecutive calls (results of
+// a call are written exactly once, by the thread owning the boundary bin or
+// by the last thread); results are visible to every thread on return.
 template <int THREADS>
-__device__ void find_boundaries(RowState& st, int nbins, int ntargets, uint32_t t0, uint32_t t1) {
+__device__ void find_boundaries_in(const uint32_t* hist, RowState& st, int nbins, int ntargets,
+                                   uint32_t t0, uint32_t t1) {
   constexpr int kWarps = THREADS / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int per = nbins / THREADS;  // nbins is 1024 or 2048, THREADS 512 or 1024
   const int b0 = tid * per;
   uint32_t local = 0;
-  for (int k = 0; k < per; ++k) local += st.hist[b0 + k];
+  for (int k = 0; k < per; ++k) local += hist[b0 + k];
   uint32_t incl = local;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const uint32_t v = __shfl_up_sync(kFull, incl, o);
     if (lane >= o) incl += v;
   }
-  if (tid < 2) {
-    st.res_bin[tid] = -1;
-    st.res_below[tid] = 0u;
-    st.res_cnt[tid] = 0u;
-  }
   if (lane == 31) st.warp_sums[warp] = incl;
   __syncthreads();
-  if (warp == 0) {
-    uint32_t w = lane < kWarps ? st.warp_sums[lane] : 0u;
+  // Every warp scans the warp totals itself (no second barrier).
+  uint32_t w = lane < kWarps ? st.warp_sums[lane] : 0u;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t v = __shfl_up_sync(kFull, w, o);
-      if (lane >= o) w += v;
-    }
-    if (lane < kWarps) st.warp_sums[lane] = w;  // inclusive over warps
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(kFull, w, o);
+    if (lane >= o) w += v;
   }
-  __syncthreads();
-  uint32_t run = (warp ? st.warp_sums[warp - 1] : 0u) + (incl - local);
+  const uint32_t before_warp = warp ? __shfl_sync(kFull, w, warp - 1) : 0u;
+  const uint32_t grand = __shfl_sync(kFull, w, kWarps - 1);
+  uint32_t run = before_warp + (incl - local);
   for (int k = 0; k < per; ++k) {
-    const uint32_t h = st.hist[b0 + k];
+    const uint32_t h = hist[b0 + k];
     const uint32_t prev = run;
     run += h;
     if (prev < t0 && t0 <= run) {
@@ -247,54 +290,311 @@ __device__ void find_boundaries(RowState& st, int nbins, int ntargets, uint32_t 
       st.res_cnt[1] = h;
     }
   }
+  if (tid == THREADS - 1) {
+    if (grand < t0) {
+      st.res_bin[0] = -1;
+      st.res_below[0] = grand;
+      st.res_cnt[0] = 0u;
+    }
+    if (ntargets > 1 && grand < t1) {
+      st.res_bin[1] = -1;
+      st.res_below[1] = grand;
+      st.res_cnt[1] = 0u;
+    }
+  }
   __syncthreads();
 }
 
+template <int THREADS>
+__device__ __forceinline__ void find_boundaries(RowState& st, int nbins, int ntargets, uint32_t t0,
+                                                uint32_t t1) {
+  find_boundaries_in<THREADS>(st.hist, st, nbins, ntargets, t0, t1);
+}
+
 // ----------------------------------------------------------------------------
-// Row scans
+// Complete-row passes
 // ----------------------------------------------------------------------------
 
-// Visits every valid element of row[lo, hi) once: 128-bit loads on the 16-byte
-// aligned body, scalar loads on the unaligned head and the tail (section 5.3).
-// fn(u, i) receives the FP32 bit pattern and the row index.
-template <int THREADS, int UNROLL, class Fn>
-__device__ __forceinline__ void for_each_in_range(const float* row, int lo, int hi, Fn&& fn) {
-  if (lo >= hi) return;
-  const int tid = threadIdx.x;
+// The 32-byte aligned body of row[lo, hi): [a0, a0 + 8 * nvec); the scalar
+// head [lo, a0) and tail [a0 + 8 * nvec, hi) hold at most 7 scores each
+// (section 5.3: wide loads on the aligned body, narrower paths for the rest).
+struct Span {
+  int a0;
+  int nvec;
+  int a_end;
+};
+
+__device__ __forceinline__ Span aligned_span(const float* row, int lo, int hi) {
   const uintptr_t addr = reinterpret_cast<uintptr_t>(row + lo);
-  // Scores are 4-byte aligned (checked on the host): at most 3 head elements.
-  int head = (int)(((16u - (uint32_t)(addr & 15u)) & 15u) >> 2);
+  int head = (int)(((32u - (uint32_t)(addr & 31u)) & 31u) >> 2);  // scores are 4-byte aligned
   if (head > hi - lo) head = hi - lo;
-  const int a0 = lo + head;
-  const int nvec = (hi - a0) >> 2;
-  const int a_end = a0 + (nvec << 2);
-  if (tid < head) fn(ld_stream1(row + lo + tid), lo + tid);
-  const uint4* v = reinterpret_cast<const uint4*>(row + a0);
-  int j = tid;
-  for (; j + (UNROLL - 1) * THREADS < nvec; j += UNROLL * THREADS) {
-    uint4 x[UNROLL];
+  Span s;
+  s.a0 = lo + head;
+  s.nvec = (hi - s.a0) >> 3;
+  s.a_end = s.a0 + (s.nvec << 3);
+  return s;
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// Per-warp stack of 8-score vectors that hold at least one admitted score:
+// kQueueCap entries of 8 bit patterns plus the vector's index in the pass.
+constexpr int kQueueCap = 32 + 32 * kTileV8;  // < 32 before a tile + one tile's pushes
+constexpr int kQueueWords = kQueueCap * 9;
+
+struct WarpQueue {
+  uint32_t* vals;  // [kQueueCap][8]
+  int32_t* vidx;   // [kQueueCap]
+};
+
+// One pass over row[lo, hi) that classifies every score by its key d into
+//   class A: d <= TA            (only when A_ON)
+//   class B: d <= TB otherwise  (TB >= TA)
+// and hands each admitted (position, index, key) to sinkA / sinkB, where the
+// position comes from the shared counter cntA / cntB.
+//
+// Streaming part, per thread: tiles of kTileV8 256-bit vectors, the next
+// tile's loads issued before the current tile is filtered.  A vector is kept
+// when its largest score passes (SIGNED_FAST: the cutoff TB is a non-negative
+// score, so "d <= TB" is the signed compare (int)u >= (int)bits(TB) on the raw
+// bits); one ballot per vector slot pushes the kept vectors onto the warp's
+// stack.  Candidate part, per warp: whenever 32 vectors are stacked, each lane
+// takes one, forms its admission mask, and the warp reserves positions with a
+// scan and one shared atomic per class.  Candidate work therefore runs with
+// full lanes instead of one lane per candidate.
+template <int THREADS, bool SIGNED_FAST, bool A_ON, class SinkA, class SinkB>
+__device__ __forceinline__ void drain_queue(const WarpQueue& q, int n, int a0, int CA, int CB,
+                                            uint32_t TA, uint32_t TB, uint32_t* cntA,
+                                            uint32_t* cntB, const SinkA& sinkA,
+                                            const SinkB& sinkB) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t lt = lanemask_lt();
+  const int j = n - 32 + lane;  // n >= 32, or a final partial drain with n < 32
+  const bool act = j >= 0;
+  uint32_t u[8];
+  int vi = 0;
+  if (act) {
+    const uint4 v0 = *reinterpret_cast<const uint4*>(q.vals + 8 * j);
+    const uint4 v1 = *reinterpret_cast<const uint4*>(q.vals + 8 * j + 4);
+    u[0] = v0.x; u[1] = v0.y; u[2] = v0.z; u[3] = v0.w;
+    u[4] = v1.x; u[5] = v1.y; u[6] = v1.z; u[7] = v1.w;
+    vi = q.vidx[j];
+  } else {
 #pragma unroll
-    for (int q = 0; q < UNROLL; ++q) x[q] = ld_stream4(v + j + q * THREADS);
+    for (int e = 0; e < 8; ++e) u[e] = SIGNED_FAST ? 0x80000000u : 0xFFFFFFFFu;
+  }
+  uint32_t m = 0u, mA = 0u;
 #pragma unroll
-    for (int q = 0; q < UNROLL; ++q) {
-      const int i = a0 + ((j + q * THREADS) << 2);
-      fn(x[q].x, i);
-      fn(x[q].y, i + 1);
-      fn(x[q].z, i + 2);
-      fn(x[q].w, i + 3);
+  for (int e = 0; e < 8; ++e) {
+    const bool adm = SIGNED_FAST ? ((int)u[e] >= CB) : (act && desc_key(u[e]) <= TB);
+    m |= adm ? (1u << e) : 0u;
+    if (A_ON) {
+      const bool a = SIGNED_FAST ? ((int)u[e] >= CA) : (desc_key(u[e]) <= TA);
+      mA |= (adm && a) ? (1u << e) : 0u;
     }
   }
-  for (; j < nvec; j += THREADS) {
-    const uint4 x = ld_stream4(v + j);
-    const int i = a0 + (j << 2);
-    fn(x.x, i);
-    fn(x.y, i + 1);
-    fn(x.z, i + 2);
-    fn(x.w, i + 3);
+  const uint32_t mB = m & ~mA;
+  const uint32_t packed = (uint32_t)__popc(mA) | ((uint32_t)__popc(mB) << 16);
+  uint32_t incl = packed;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
   }
-  const int t = a_end + tid;
-  if (t < hi) fn(ld_stream1(row + t), t);
+  const uint32_t total = __shfl_sync(kFull, incl, 31);
+  uint32_t bA = 0u, bB = 0u;
+  if (lane == 0) {
+    if (A_ON && (total & 0xFFFFu)) bA = atomicAdd(cntA, total & 0xFFFFu);
+    if (total >> 16) bB = atomicAdd(cntB, total >> 16);
+  }
+  if (A_ON) bA = __shfl_sync(kFull, bA, 0);
+  bB = __shfl_sync(kFull, bB, 0);
+  const uint32_t excl = incl - packed;
+  uint32_t pA = bA + (excl & 0xFFFFu), pB = bB + (excl >> 16);
+  (void)lt;
+  const int ibase = a0 + 8 * vi;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    if (m & (1u << e)) {
+      const uint32_t d = desc_key(u[e]);
+      if (A_ON && (mA & (1u << e)))
+        sinkA(pA++, ibase + e, d);
+      else
+        sinkB(pB++, ibase + e, d);
+    }
+  }
 }
+
+template <int THREADS, bool SIGNED_FAST, bool A_ON, class SinkA, class SinkB>
+__device__ __forceinline__ void scan_tiles(const float* row, int lo, int hi, uint32_t TA,
+                                           uint32_t TB, uint32_t* cntA, uint32_t* cntB,
+                                           uint32_t* queues, const SinkA& sinkA,
+                                           const SinkB& sinkB) {
+  if (lo >= hi) return;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const Span sp = aligned_span(row, lo, hi);
+  const int head = sp.a0 - lo, tail = hi - sp.a_end;
+  if (tid < head + tail) {
+    const int i = tid < head ? lo + tid : sp.a_end + (tid - head);
+    const uint32_t d = desc_key(ld_stream1(row + i));
+    if (d <= TB) {
+      if (A_ON && d <= TA)
+        sinkA(atomicAdd(cntA, 1u), i, d);
+      else
+        sinkB(atomicAdd(cntB, 1u), i, d);
+    }
+  }
+  const int CB = (int)bits_from_desc(TB);
+  const int CA = (int)bits_from_desc(TA);
+  const uint32_t lt = lanemask_lt();
+  WarpQueue q;
+  q.vals = queues + (tid >> 5) * kQueueWords;
+  q.vidx = reinterpret_cast<int32_t*>(q.vals + kQueueCap * 8);
+  int qn = 0;  // warp-uniform stack depth
+  const float* body = row + sp.a0;
+  constexpr int kStep = kTileV8 * THREADS;
+  constexpr uint32_t kSentinel = SIGNED_FAST ? 0x80000000u : 0xFFFFFFFFu;
+  uint32_t x[kTileScores];
+#pragma unroll
+  for (int g = 0; g < kTileV8; ++g) {
+    const int idx = g * THREADS + tid;
+    if (idx < sp.nvec) {
+      ld_stream8(body + 8 * idx, &x[8 * g]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) x[8 * g + k] = kSentinel;
+    }
+  }
+  for (int t = 0; t < sp.nvec; t += kStep) {
+    uint32_t y[kTileScores];
+    const bool more = t + kStep < sp.nvec;
+#pragma unroll
+    for (int g = 0; g < kTileV8; ++g) {
+      const int idx = t + kStep + g * THREADS + tid;
+      if (more && idx < sp.nvec) {
+        ld_stream8(body + 8 * idx, &y[8 * g]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) y[8 * g + k] = kSentinel;
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < kTileV8; ++g) {
+      const int vi = t + g * THREADS + tid;
+      bool keep;
+      if (SIGNED_FAST) {
+        int mx = (int)x[8 * g];
+#pragma unroll
+        for (int k = 1; k < 8; ++k) mx = max(mx, (int)x[8 * g + k]);
+        keep = mx >= CB;
+      } else {
+        uint32_t mn = desc_key(x[8 * g]);
+#pragma unroll
+        for (int k = 1; k < 8; ++k) mn = min(mn, desc_key(x[8 * g + k]));
+        keep = vi < sp.nvec && mn <= TB;
+      }
+      const uint32_t bal = __ballot_sync(kFull, keep);
+      if (bal != 0u) {
+        if (keep) {
+          const int pos = qn + __popc(bal & lt);
+          uint4* dst = reinterpret_cast<uint4*>(q.vals + 8 * pos);
+          dst[0] = make_uint4(x[8 * g], x[8 * g + 1], x[8 * g + 2], x[8 * g + 3]);
+          dst[1] = make_uint4(x[8 * g + 4], x[8 * g + 5], x[8 * g + 6], x[8 * g + 7]);
+          q.vidx[pos] = vi;
+        }
+        qn += __popc(bal);
+      }
+    }
+    if (qn >= 32) {
+      __syncwarp();
+      do {
+        drain_queue<THREADS, SIGNED_FAST, A_ON>(q, qn, sp.a0, CA, CB, TA, TB, cntA, cntB, sinkA,
+                                                sinkB);
+        qn -= 32;
+      } while (qn >= 32);
+      __syncwarp();
+    }
+#pragma unroll
+    for (int k = 0; k < kTileScores; ++k) x[k] = y[k];
+  }
+  if (qn > 0) {
+    __syncwarp();
+    drain_queue<THREADS, SIGNED_FAST, A_ON>(q, qn, sp.a0, CA, CB, TA, TB, cntA, cntB, sinkA,
+                                            sinkB);
+    __syncwarp();
+  }
+}
+
+// Dispatches on the cutoff's sign (signed-compare fast path) and on whether
+// class A exists.
+template <int THREADS, class SinkA, class SinkB>
+__device__ __forceinline__ void scan_two_class(const float* row, int lo, int hi, uint32_t TA,
+                                               uint32_t TB, bool a_on, uint32_t* cntA,
+                                               uint32_t* cntB, uint32_t* queues,
+                                               const SinkA& sinkA, const SinkB& sinkB) {
+  const bool fast = (bits_from_desc(TB) & 0x80000000u) == 0u;
+  if (fast) {
+    if (a_on)
+      scan_tiles<THREADS, true, true>(row, lo, hi, TA, TB, cntA, cntB, queues, sinkA, sinkB);
+    else
+      scan_tiles<THREADS, true, false>(row, lo, hi, TA, TB, cntA, cntB, queues, sinkA, sinkB);
+  } else {
+    if (a_on)
+      scan_tiles<THREADS, false, true>(row, lo, hi, TA, TB, cntA, cntB, queues, sinkA, sinkB);
+    else
+      scan_tiles<THREADS, false, false>(row, lo, hi, TA, TB, cntA, cntB, queues, sinkA, sinkB);
+  }
+}
+
+// Coarse histogram over row[lo, hi) (first pass of exact coarse recovery, eq. 20).
+template <int THREADS>
+__device__ void scan_coarse_hist(const float* row, int lo, int hi, RowState& st) {
+  if (lo >= hi) return;
+  const int tid = threadIdx.x;
+  const Span sp = aligned_span(row, lo, hi);
+  const int head = sp.a0 - lo, tail = hi - sp.a_end;
+  if (tid < head + tail) {
+    const int i = tid < head ? lo + tid : sp.a_end + (tid - head);
+    atomicAdd(&st.hist[coarse_bin(ld_stream1(row + i))], 1u);
+  }
+  const float* body = row + sp.a0;
+  for (int t = tid; t < sp.nvec; t += 2 * THREADS) {
+    uint32_t x[16];
+    const bool second = t + THREADS < sp.nvec;
+    ld_stream8(body + 8 * t, x);
+    if (second) ld_stream8(body + 8 * (t + THREADS), x + 8);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) atomicAdd(&st.hist[coarse_bin(x[k])], 1u);
+    if (second) {
+#pragma unroll
+      for (int k = 8; k < 16; ++k) atomicAdd(&st.hist[coarse_bin(x[k])], 1u);
+    }
+  }
+}
+
+// Sinks: where an admitted (position, index, key) goes.
+struct FrontierSink {  // frontier entry + leading-digit histogram (eqs. 17, 20)
+  Frontier F;
+  uint32_t* hist;
+  __device__ __forceinline__ void operator()(uint32_t p, int32_t i, uint32_t d) const {
+    F.put(p, i, d);
+    atomicAdd(&hist[d >> 21], 1u);
+  }
+};
+struct CommitSink {  // committed straight to the output (E0 of eq. 20)
+  int32_t* out_row;
+  uint32_t K;
+  __device__ __forceinline__ void operator()(uint32_t p, int32_t i, uint32_t) const {
+    if (p < K) out_row[p] = i;
+  }
+};
+struct DropSink {
+  __device__ __forceinline__ void operator()(uint32_t, int32_t, uint32_t) const {}
+};
 
 // Output slot reservation for one committed index.
 __device__ __forceinline__ void commit(RowState& st, int32_t* out_row, int K, int32_t i) {
@@ -302,59 +602,17 @@ __device__ __forceinline__ void commit(RowState& st, int32_t* out_row, int K, in
   if (slot < (uint32_t)K) out_row[slot] = i;
 }
 
-// Phase 2 (section 4.3, eq. 16-17; section 5.3): one pass over row[lo, hi)
-// admits every index whose key d lies in [dlo, dlo + dspan], appends (i, d) to
-// the frontier and adds digit 0 of d to the shared histogram.
-template <int THREADS>
-__device__ void scan_admit(const float* row, int lo, int hi, uint32_t dlo, uint32_t dspan,
-                           const Frontier& F, RowState& st) {
-  for_each_in_range<THREADS, 4>(row, lo, hi, [&](uint32_t u, int i) {
-    const uint32_t d = desc_key(u);
-    if (d - dlo <= dspan) {
-      const uint32_t p = atomicAdd(&st.n_front, 1u);
-      F.put(p, i, d);
-      atomicAdd(&st.hist[d >> 21], 1u);
-    }
-  });
-}
-
-// Coarse histogram over row[lo, hi) (first pass of exact coarse recovery, eq. 20).
-template <int THREADS>
-__device__ void scan_coarse_hist(const float* row, int lo, int hi, RowState& st) {
-  for_each_in_range<THREADS, 4>(row, lo, hi, [&](uint32_t u, int i) {
-    atomicAdd(&st.hist[coarse_bin(u, desc_key(u))], 1u);
-  });
-}
-
-// Second pass of exact coarse recovery (eq. 20): keys d <= tlo (c < tau*) are
-// committed to the output (E0), keys in (tlo, thi] (c == tau*) form Q0 and h0.
-template <int THREADS>
-__device__ void scan_exact_classify(const float* row, int lo, int hi, bool has_lo, uint32_t tlo,
-                                    uint32_t thi, const Frontier& F, RowState& st, int32_t* out_row,
-                                    int K) {
-  for_each_in_range<THREADS, 4>(row, lo, hi, [&](uint32_t u, int i) {
-    const uint32_t d = desc_key(u);
-    if (d <= thi) {
-      if (has_lo && d <= tlo) {
-        commit(st, out_row, K, i);
-      } else {
-        const uint32_t p = atomicAdd(&st.n_front, 1u);
-        F.put(p, i, d);
-        atomicAdd(&st.hist[d >> 21], 1u);
-      }
-    }
-  });
-}
-
 // ----------------------------------------------------------------------------
 // Phase 3: prefix-commit-retain refinement (section 4.4, eqs. 22-25)
 // ----------------------------------------------------------------------------
 
+// General form for frontiers that spill to global memory: in-place chunked
+// compaction of the frontier at every digit.
 // Entry: frontier holds n entries (Q0), st.hist holds h0 (digit 0 over Q0),
 // k = k0 indices remain to be selected, st.n_out = |E0|.  Exit: st.n_out == K.
 template <int THREADS>
-__device__ void refine(const Frontier& F, uint32_t n, uint32_t k, RowState& st, int32_t* out_row,
-                       int K) {
+__device__ void refine_general(const Frontier& F, uint32_t n, uint32_t k, RowState& st,
+                               int32_t* out_row, int K) {
   constexpr int R = 4;
   constexpr uint32_t CH = THREADS * R;
   const int tid = threadIdx.x;
@@ -443,6 +701,118 @@ __device__ void refine(const Frontier& F, uint32_t n, uint32_t k, RowState& st, 
   __syncthreads();
 }
 
+// Warp-aggregated commit of idx for the lanes where `com` holds.
+__device__ __forceinline__ void commit_warp(RowState& st, int32_t* out_row, int K, bool com,
+                                            int32_t idx, uint32_t lt) {
+  const uint32_t bal = __ballot_sync(kFull, com);
+  if (bal == 0u) return;
+  uint32_t base = 0u;
+  if ((threadIdx.x & 31) == 0) base = atomicAdd(&st.n_out, (uint32_t)__popc(bal));
+  base = __shfl_sync(kFull, base, 0);
+  if (com) {
+    const uint32_t slot = base + (uint32_t)__popc(bal & lt);
+    if (slot < (uint32_t)K) out_row[slot] = idx;
+  }
+}
+
+// Phase 3 (section 4.4, eqs. 22-25) with the frontier resident in registers:
+// each thread holds up to 8 (index, key) entries, so no entry moves between
+// digits; the histogram of the next digit is built in a second buffer while
+// the current digit is classified.  Same entry and exit conditions as
+// refine_general, to which frontiers beyond shared memory are handed.
+template <int THREADS>
+__device__ void refine(const Frontier& F, uint32_t n, uint32_t k, RowState& st, int32_t* out_row,
+                       int K) {
+  constexpr int EPT = 8;
+  if (n > F.cap || F.cap > (uint32_t)(EPT * THREADS)) {
+    refine_general<THREADS>(F, n, k, st, out_row, K);
+    return;
+  }
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t lt = lanemask_lt();
+  uint32_t key[EPT];
+  int32_t idx[EPT];
+  uint32_t alive = 0u;
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) {
+    const uint32_t p = (uint32_t)(e * THREADS + tid);
+    if (p < n) {
+      const uint2 v = F.s[p];
+      idx[e] = (int32_t)v.x;
+      key[e] = v.y;
+      alive |= 1u << e;
+    } else {
+      idx[e] = -1;
+      key[e] = 0xFFFFFFFFu;
+    }
+  }
+  uint32_t* hc = st.hist;
+  uint32_t* hn = st.hist2;
+  for (int q = tid; q < 2048; q += THREADS) hn[q] = 0u;
+  __syncthreads();
+  for (int j = 0; j < 3 && k > 0; ++j) {
+    find_boundaries_in<THREADS>(hc, st, j == 2 ? 1024 : 2048, 1, k, 0u);
+    const int b = st.res_bin[0];
+    const uint32_t below = st.res_below[0], cnt = st.res_cnt[0];
+    if (b < 0) {  // inconsistent counts: cannot happen; finish_row flags it
+      k = 0;
+      break;
+    }
+    // b_j = min{b : H_j(b) >= k_j} (eq. 23); commit digit < b_j (eq. 24), keep
+    // digit == b_j (eq. 25).  When H_j(b_j) == k_j the boundary group closes
+    // the quota and is committed too.
+    const bool last = below + cnt == k;
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
+      const bool al = (alive >> e) & 1u;
+      const int dg = (int)digit(key[e], j);
+      const bool com = al && (last ? dg <= b : dg < b);
+      const bool keep = al && !last && dg == b;
+      commit_warp(st, out_row, K, com, idx[e], lt);
+      if (keep && j < 2) atomicAdd(&hn[digit(key[e], j + 1)], 1u);
+      if (!keep) alive &= ~(1u << e);
+    }
+    if (last) {
+      k = 0;
+      break;
+    }
+    k -= below;
+    __syncthreads();  // next histogram complete; the finder is done with hc
+    uint32_t* t = hc;
+    hc = hn;
+    hn = t;
+    if (j < 1)
+      for (int q = tid; q < 2048; q += THREADS) hn[q] = 0u;  // ordered by the next finder's barrier
+  }
+  if (k > 0) {
+    // After the last digit every alive key is identical: take the first k in
+    // (thread, slot) order.
+    const uint32_t c = (uint32_t)__popc(alive);
+    uint32_t incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) st.warp_sums[warp] = incl;
+    __syncthreads();
+    uint32_t w = lane < THREADS / 32 ? st.warp_sums[lane] : 0u;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(kFull, w, o);
+      if (lane >= o) w += v;
+    }
+    uint32_t rank = (warp ? __shfl_sync(kFull, w, warp - 1) : 0u) + incl - c;
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
+      const bool al = (alive >> e) & 1u;
+      commit_warp(st, out_row, K, al && rank < k, idx[e], lt);
+      rank += al ? 1u : 0u;
+    }
+  }
+  __syncthreads();
+}
+
 // ----------------------------------------------------------------------------
 // Row-level building blocks
 // ----------------------------------------------------------------------------
@@ -478,6 +848,21 @@ __device__ void finish_row(const Params& p, RowState& st, int32_t* out_row) {
   __syncthreads();
 }
 
+// Cutoffs of the exact coarse boundary tau* (warps 0 and 1 in parallel):
+// cut[1] admits c <= tau*, cut[0] admits c < tau* (none when tau* == 0).
+template <int THREADS>
+__device__ void exact_cutoffs(RowState& st, int tstar) {
+  const int warp = threadIdx.x >> 5;
+  if (warp == 0) {
+    const uint32_t t = cutoff_for_bin_warp(tstar);
+    if ((threadIdx.x & 31) == 0) st.cut[1] = t;
+  } else if (warp == 1) {
+    const uint32_t t = tstar > 0 ? cutoff_for_bin_warp(tstar - 1) : 0u;
+    if ((threadIdx.x & 31) == 0) st.cut[0] = t;
+  }
+  __syncthreads();
+}
+
 // Exact coarse recovery over row[0, L) followed by refinement (eq. 20).
 // Leaves st.n_out == K.  Returns tau*, |E0| and |Q0| through the out params.
 template <int THREADS>
@@ -495,15 +880,14 @@ __device__ void exact_route(const Params& p, const float* row, int L, const Fron
   find_boundaries<THREADS>(st, 2048, 1, (uint32_t)K, 0u);
   tstar = st.res_bin[0];
   e0 = (int)st.res_below[0];
-  if (threadIdx.x == 0) {
-    st.cut[1] = cutoff_for_bin(tstar);
-  } else if (threadIdx.x == 32) {
-    st.cut[0] = tstar > 0 ? cutoff_for_bin(tstar - 1) : 0u;
-  }
-  __syncthreads();
+  exact_cutoffs<THREADS>(st, tstar);
+  const uint32_t tlo = st.cut[0], thi = st.cut[1];
   clear_hist<THREADS>(st, 2048);
   __syncthreads();
-  scan_exact_classify<THREADS>(row, 0, L, tstar > 0, st.cut[0], st.cut[1], F, st, out_row, K);
+  CommitSink commit_sink{out_row, (uint32_t)K};
+  FrontierSink front_sink{F, st.hist};
+  scan_two_class<THREADS>(row, 0, L, tlo, thi, tstar > 0, &st.n_out, &st.n_front, queue_area(p), commit_sink,
+                          front_sink);
   __syncthreads();
   q0n = (int)st.n_front;
   refine<THREADS>(F, st.n_front, (uint32_t)(K - e0), st, out_row, K);
@@ -518,19 +902,15 @@ __device__ void exact_route_resident(const Params& p, const float* row, int L, c
   const int K = p.K;
   const int tid = threadIdx.x;
   uint32_t v[VPT];
-  const bool aligned = (reinterpret_cast<uintptr_t>(row) & 15u) == 0u;
+  const bool aligned = (reinterpret_cast<uintptr_t>(row) & 31u) == 0u;
 #pragma unroll
-  for (int g = 0; g < VPT / 4; ++g) {
-    const int i0 = (g * THREADS + tid) * 4;
-    if (aligned && i0 + 3 < L) {
-      const uint4 x = ld_stream4(reinterpret_cast<const uint4*>(row + i0));
-      v[g * 4 + 0] = x.x;
-      v[g * 4 + 1] = x.y;
-      v[g * 4 + 2] = x.z;
-      v[g * 4 + 3] = x.w;
+  for (int g = 0; g < VPT / 8; ++g) {
+    const int i0 = (g * THREADS + tid) * 8;
+    if (aligned && i0 + 7 < L) {
+      ld_stream8(row + i0, v + 8 * g);
     } else {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) v[g * 4 + e] = (i0 + e < L) ? ld_stream1(row + i0 + e) : 0u;
+      for (int e = 0; e < 8; ++e) v[g * 8 + e] = (i0 + e < L) ? ld_stream1(row + i0 + e) : 0u;
     }
   }
   clear_hist<THREADS>(st, 2048);
@@ -540,34 +920,29 @@ __device__ void exact_route_resident(const Params& p, const float* row, int L, c
   }
   __syncthreads();
 #pragma unroll
-  for (int g = 0; g < VPT / 4; ++g) {
+  for (int g = 0; g < VPT / 8; ++g) {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int i = (g * THREADS + tid) * 4 + e;
-      if (i < L) atomicAdd(&st.hist[coarse_bin(v[g * 4 + e], desc_key(v[g * 4 + e]))], 1u);
+    for (int e = 0; e < 8; ++e) {
+      const int i = (g * THREADS + tid) * 8 + e;
+      if (i < L) atomicAdd(&st.hist[coarse_bin(v[g * 8 + e])], 1u);
     }
   }
   __syncthreads();
   find_boundaries<THREADS>(st, 2048, 1, (uint32_t)K, 0u);
   tstar = st.res_bin[0];
   e0 = (int)st.res_below[0];
-  if (tid == 0) {
-    st.cut[1] = cutoff_for_bin(tstar);
-  } else if (tid == 32) {
-    st.cut[0] = tstar > 0 ? cutoff_for_bin(tstar - 1) : 0u;
-  }
-  __syncthreads();
+  exact_cutoffs<THREADS>(st, tstar);
   clear_hist<THREADS>(st, 2048);
   __syncthreads();
   const uint32_t tlo = st.cut[0], thi = st.cut[1];
   const bool has_lo = tstar > 0;
 #pragma unroll
-  for (int g = 0; g < VPT / 4; ++g) {
+  for (int g = 0; g < VPT / 8; ++g) {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int i = (g * THREADS + tid) * 4 + e;
+    for (int e = 0; e < 8; ++e) {
+      const int i = (g * THREADS + tid) * 8 + e;
       if (i < L) {
-        const uint32_t d = desc_key(v[g * 4 + e]);
+        const uint32_t d = desc_key(v[g * 8 + e]);
         if (d <= thi) {
           if (has_lo && d <= tlo) {
             commit(st, out_row, K, i);
@@ -596,20 +971,33 @@ __device__ __forceinline__ int view_size(int L, int a, int s) {
 
 // Phase 1 (section 4.2, eqs. 13-15): coarse histogram of the view
 // V = {i < L : i = a_r (mod s)} and the boundaries tau0 / tau1 with their
-// inclusive cutoffs.  Entered with a cleared histogram; leaves it dirty.
+// inclusive cutoffs.  Each thread issues up to 8 view loads before using any.
+// Entered with a cleared histogram; leaves it dirty.
 template <int THREADS>
 __device__ void sample_view(const Params& p, const float* row, int L, int a, RowState& st) {
-  for (int t = threadIdx.x;; t += THREADS) {
-    const int64_t i = (int64_t)a + (int64_t)t * p.s;
-    if (i >= L) break;
-    const uint32_t u = ld_stream1(row + i);
-    atomicAdd(&st.hist[coarse_bin(u, desc_key(u))], 1u);
+  const int nv = view_size(L, a, p.s);
+  const int tid = threadIdx.x;
+  for (int t0 = 0; t0 < nv; t0 += 8 * THREADS) {
+    uint32_t u[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int t = t0 + k * THREADS + tid;
+      u[k] = t < nv ? __ldg(reinterpret_cast<const unsigned int*>(row) + a + (int64_t)t * p.s) : 0u;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (t0 + k * THREADS + tid < nv) atomicAdd(&st.hist[coarse_bin(u[k])], 1u);
   }
   __syncthreads();
   find_boundaries<THREADS>(st, 2048, 2, (uint32_t)p.q0, (uint32_t)p.q1);
-  const int tid = threadIdx.x;
-  if (tid == 0) st.cut[0] = cutoff_for_bin(st.res_bin[0]);
-  if (tid == 32 && p.dual) st.cut[1] = cutoff_for_bin(st.res_bin[1]);
+  const int warp = tid >> 5;
+  if (warp == 0) {
+    const uint32_t t = cutoff_for_bin_warp(st.res_bin[0]);
+    if ((tid & 31) == 0) st.cut[0] = t;
+  } else if (warp == 1 && p.dual) {
+    const uint32_t t = cutoff_for_bin_warp(st.res_bin[1]);
+    if ((tid & 31) == 0) st.cut[1] = t;
+  }
   __syncthreads();
 }
 
@@ -630,14 +1018,17 @@ __device__ bool guess_bin(const Params& p, const float* row, int L, int r, RowSt
       invalid = 1;
     } else {
       const uint32_t u = __ldg(reinterpret_cast<const unsigned int*>(row) + idx);
-      worst = max(worst, coarse_bin(u, desc_key(u)));
+      worst = max(worst, coarse_bin(u));
     }
   }
   if (invalid) atomicOr(&st.ginvalid, 1);
   if (worst >= 0) atomicMax(&st.gmax, worst);
   __syncthreads();
   const bool ok = st.ginvalid == 0;
-  if (ok && threadIdx.x == 0) st.cut[0] = cutoff_for_bin(st.gmax);
+  if (ok && threadIdx.x < 32) {
+    const uint32_t t = cutoff_for_bin_warp(st.gmax);
+    if (threadIdx.x == 0) st.cut[0] = t;
+  }
   __syncthreads();
   return ok;
 }
@@ -660,14 +1051,19 @@ __device__ void sampled_row(const Params& p, int r, const Frontier& F, RowState&
   if (threadIdx.x == 0) {
     st.n_front = 0u;
     st.n_out = 0u;
+    st.n_drop = 0u;
   }
   __syncthreads();
 
+  FrontierSink front_sink{F, st.hist};
+  DropSink drop;
   int route = -1, tau0 = -1, tau1 = -1, c0 = -1, c1 = -1;
   bool certified = false;
   if (p.prev != nullptr && guess_bin<THREADS>(p, row, L, r, st)) {
     tau0 = st.gmax;
-    scan_admit<THREADS>(row, 0, L, 0u, st.cut[0], F, st);
+    const uint32_t T = st.cut[0];
+    scan_two_class<THREADS>(row, 0, L, T, T, false, &st.n_drop, &st.n_front, queue_area(p), drop,
+                            front_sink);
     __syncthreads();
     c0 = (int)st.n_front;
     certified = c0 >= K;
@@ -683,15 +1079,19 @@ __device__ void sampled_row(const Params& p, int r, const Frontier& F, RowState&
       const uint32_t T0 = st.cut[0], T1 = st.cut[1];
       clear_hist<THREADS>(st, 2048);
       __syncthreads();
-      scan_admit<THREADS>(row, 0, L, 0u, T0, F, st);  // Phase 2
+      // Phase 2: admit d <= T0, persist candidates, build h0 (eqs. 16-17).
+      scan_two_class<THREADS>(row, 0, L, T0, T0, false, &st.n_drop, &st.n_front, queue_area(p),
+                              drop, front_sink);
       __syncthreads();
       c0 = (int)st.n_front;
       if (c0 >= K) {
         route = EXACT_TOPK_ROUTE_PRIMARY;
         certified = true;
       } else if (p.dual) {
-        // Band rescue (eqs. 18-19): append only T0 < d <= T1.
-        if (T1 > T0) scan_admit<THREADS>(row, 0, L, T0 + 1u, T1 - T0 - 1u, F, st);
+        // Band rescue (eqs. 18-19): a second pass appends only T0 < d <= T1.
+        if (T1 > T0)
+          scan_two_class<THREADS>(row, 0, L, T0, T1, true, &st.n_drop, &st.n_front, queue_area(p), drop,
+                                  front_sink);
         __syncthreads();
         c1 = (int)st.n_front;
         certified = c1 >= K;
@@ -733,26 +1133,21 @@ __device__ __forceinline__ int live_rows(const Params& p) {
   return m < 0 ? 0 : (m > p.M_cap ? p.M_cap : m);
 }
 
-template <int THREADS>
 __device__ __forceinline__ RowState& row_state() {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   return *reinterpret_cast<RowState*>(smem_raw);
 }
 
-template <int THREADS>
 __device__ __forceinline__ Frontier make_frontier(const Params& p, int64_t slice) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Frontier F;
-  F.s_idx = reinterpret_cast<int32_t*>(smem_raw + sizeof(RowState));
-  F.s_key = reinterpret_cast<uint32_t*>(smem_raw + sizeof(RowState) + sizeof(int32_t) * p.cap);
+  F.s = reinterpret_cast<uint2*>(smem_raw + sizeof(RowState));
   F.cap = (uint32_t)p.cap;
-  if (p.ws_idx != nullptr) {
-    F.g_idx = p.ws_idx + slice * p.N;
-    F.g_key = p.ws_key + slice * p.N;
+  if (p.ws != nullptr) {
+    F.g = p.ws + slice * p.N;
     F.gcap = (uint32_t)p.N;
   } else {
-    F.g_idx = nullptr;
-    F.g_key = nullptr;
+    F.g = nullptr;
     F.gcap = 0u;
   }
   return F;
@@ -762,9 +1157,9 @@ __device__ __forceinline__ Frontier make_frontier(const Params& p, int64_t slice
 // Kernel 1: persistent sampled
 // ----------------------------------------------------------------------------
 
-__global__ void __launch_bounds__(kPersistentThreads, 3) persistent_sampled_kernel(Params p) {
-  RowState& st = row_state<kPersistentThreads>();
-  const Frontier F = make_frontier<kPersistentThreads>(p, blockIdx.x);
+__global__ void __launch_bounds__(kPersistentThreads, ETK_SAMPLED_MIN_CTAS) persistent_sampled_kernel(Params p) {
+  RowState& st = row_state();
+  const Frontier F = make_frontier(p, blockIdx.x);
   const int M = live_rows(p);
   int r = blockIdx.x;
   while (r < M) {
@@ -782,8 +1177,8 @@ __global__ void __launch_bounds__(kPersistentThreads, 3) persistent_sampled_kern
 // ----------------------------------------------------------------------------
 
 __global__ void __launch_bounds__(kRowLocalThreads, 1) row_local_exact_kernel(Params p) {
-  RowState& st = row_state<kRowLocalThreads>();
-  const Frontier F = make_frontier<kRowLocalThreads>(p, blockIdx.x);
+  RowState& st = row_state();
+  const Frontier F = make_frontier(p, blockIdx.x);
   const int M = live_rows(p);
   int r = blockIdx.x;
   while (r < M) {
@@ -817,18 +1212,36 @@ __global__ void __launch_bounds__(kRowLocalThreads, 1) row_local_exact_kernel(Pa
 // Kernel 3: KV-split sampled (section 4.5 eqs. 26-27; section 5.5)
 // ----------------------------------------------------------------------------
 
-// Segment p of a row of length L: contiguous, 4-float aligned starts.
+// Segment p of a row of length L: contiguous, starts 8-float (32-byte) aligned
+// relative to the row start.
 __device__ __forceinline__ void segment_bounds(int L, int P, int p, int& lo, int& hi) {
   int seg = (L + P - 1) / P;
-  seg = (seg + 3) & ~3;
+  seg = (seg + 7) & ~7;
   const int64_t a = (int64_t)p * seg;
   lo = a > L ? L : (int)a;
   const int64_t b = a + seg;
   hi = b > L ? L : (int)b;
 }
 
-__global__ void __launch_bounds__(kKvSplitThreads, 3) kv_split_kernel(Params p) {
-  RowState& st = row_state<kKvSplitThreads>();
+// Segment candidate sinks: primary entries fill the segment's range of the row
+// buffer from its start, band entries from its end.
+struct SegmentFrontSink {
+  uint2* rb;
+  int lo;
+  __device__ __forceinline__ void operator()(uint32_t p, int32_t i, uint32_t d) const {
+    rb[lo + (int)p] = make_uint2((uint32_t)i, d);
+  }
+};
+struct SegmentBackSink {
+  uint2* rb;
+  int hi;
+  __device__ __forceinline__ void operator()(uint32_t p, int32_t i, uint32_t d) const {
+    rb[hi - 1 - (int)p] = make_uint2((uint32_t)i, d);
+  }
+};
+
+__global__ void __launch_bounds__(kKvSplitThreads, ETK_SAMPLED_MIN_CTAS) kv_split_kernel(Params p) {
+  RowState& st = row_state();
   const int r = blockIdx.y;
   const int seg = blockIdx.x;
   const int P = p.P;
@@ -840,9 +1253,8 @@ __global__ void __launch_bounds__(kKvSplitThreads, 3) kv_split_kernel(Params p) 
   L = L < 0 ? 0 : (L > p.N ? p.N : L);
   int32_t* out_row = p.out + (int64_t)r * K;
   // Row buffer: segment-owned candidate ranges, later the finisher's spill.
-  int32_t* rb_idx = p.ws_idx + (int64_t)r * p.N;
-  uint32_t* rb_key = p.ws_key + (int64_t)r * p.N;
-  Frontier F = make_frontier<kKvSplitThreads>(p, r);
+  uint2* rb = p.ws + (int64_t)r * p.N;
+  const Frontier F = make_frontier(p, r);
 
   if (L <= K) {
     if (seg == 0) {
@@ -891,27 +1303,20 @@ __global__ void __launch_bounds__(kKvSplitThreads, 3) kv_split_kernel(Params p) 
     use_band = p.dual && T1 > T0;
   }
 
-  // Phase 2 over this segment: primary candidates fill the segment's range
-  // from its start, band candidates (T0 < d <= T1) from its end, so the band
-  // costs no second traversal.
+  // Phase 2 over this segment, with the band (T0 < d <= T1) collected in the
+  // same traversal: an underfilled primary needs no second pass.
   int lo, hi;
   segment_bounds(L, P, seg, lo, hi);
-  for_each_in_range<kKvSplitThreads, 4>(row, lo, hi, [&](uint32_t u, int i) {
-    const uint32_t d = desc_key(u);
-    if (d <= T0) {
-      const uint32_t q = atomicAdd(&st.seg_c0, 1u);
-      rb_idx[lo + q] = i;
-      rb_key[lo + q] = d;
-    } else if (use_band && d <= T1) {
-      const uint32_t q = atomicAdd(&st.seg_cb, 1u);
-      rb_idx[hi - 1 - q] = i;
-      rb_key[hi - 1 - q] = d;
-    }
-  });
+  {
+    SegmentFrontSink primary{rb, lo};
+    SegmentBackSink band{rb, hi};
+    scan_two_class<kKvSplitThreads>(row, lo, hi, T0, use_band ? T1 : T0, true, &st.seg_c0,
+                                    &st.seg_cb, queue_area(p), primary, band);
+  }
   __threadfence();  // every writer publishes its candidates before the arrival
   __syncthreads();
-  int32_t* counts = p.seg_counts + ((int64_t)r * P + seg) * 2;
   if (tid == 0) {
+    int32_t* counts = p.seg_counts + ((int64_t)r * P + seg) * 2;
     counts[0] = (int32_t)st.seg_c0;
     counts[1] = (int32_t)st.seg_cb;
     __threadfence();
@@ -924,12 +1329,28 @@ __global__ void __launch_bounds__(kKvSplitThreads, 3) kv_split_kernel(Params p) 
   // ---- finisher: merge (eq. 27), certify, refine or recover ----
   __threadfence();
   if (tid == 0) atomicExch(p.counters + kCtrArriveBase + r, 0);
-  uint32_t c0 = 0u, cb = 0u;
-  for (int q = 0; q < P; ++q) {
+  for (int q = tid; q < P; q += kKvSplitThreads) {
     const int32_t* cq = p.seg_counts + ((int64_t)r * P + q) * 2;
-    c0 += (uint32_t)__ldcg(cq);
-    cb += (uint32_t)__ldcg(cq + 1);
+    st.run_c0[q] = (uint32_t)__ldcg(cq);
+    st.run_cb[q] = (uint32_t)__ldcg(cq + 1);
   }
+  __syncthreads();
+  if (tid < 32) {
+    // Totals of both counts, each lane summing up to 4 consecutive segments.
+    uint32_t s0 = 0u, sb = 0u;
+    for (int q = tid * 4; q < tid * 4 + 4 && q < P; ++q) {
+      s0 += st.run_c0[q];
+      sb += st.run_cb[q];
+    }
+    s0 = __reduce_add_sync(kFull, s0);
+    sb = __reduce_add_sync(kFull, sb);
+    if (tid == 0) {
+      st.tot_c0 = s0;
+      st.tot_cb = sb;
+    }
+  }
+  __syncthreads();
+  const uint32_t c0 = st.tot_c0, cb = st.tot_cb;
   int route;
   bool certified;
   bool with_band = false;
@@ -950,17 +1371,25 @@ __global__ void __launch_bounds__(kKvSplitThreads, 3) kv_split_kernel(Params p) 
   const int c1 = with_band ? (int)(c0 + cb) : -1;
   int tstar = -1, e0 = 0, q0n;
   if (certified) {
-    // Gather the runs (segment p's primary range, then its band range) into
-    // the frontier, in order.  Logical position f maps to shared memory below
-    // cap and to rb[f] above; every source position is >= the number of
-    // entries gathered before it, so chunked in-place gathering never
-    // overwrites an unread entry.
-    const uint32_t total = with_band ? c0 + cb : c0;
+    // Run table: segment q contributes its primary range then (band route)
+    // its band range, in segment order.
+    if (tid == 0) {
+      uint32_t acc = 0u;
+      for (int q = 0; q < P; ++q) {
+        st.run_pre[q] = acc;
+        acc += st.run_c0[q] + (with_band ? st.run_cb[q] : 0u);
+      }
+      st.run_pre[P] = acc;
+    }
     clear_hist<kKvSplitThreads>(st, 2048);
     __syncthreads();
+    // Gather the runs into the frontier in order.  Logical position f maps to
+    // shared memory below cap and to rb[f] above; every source position is >=
+    // its logical position, so gathering in chunks (read all, then write)
+    // never overwrites an unread entry.
+    const uint32_t total = st.run_pre[P];
     constexpr int R = 4;
     constexpr uint32_t CH = kKvSplitThreads * R;
-    // run walk state per thread is recomputed per element: runs are few.
     for (uint32_t c = 0; c < total; c += CH) {
       int32_t idx[R];
       uint32_t key[R];
@@ -969,24 +1398,26 @@ __global__ void __launch_bounds__(kKvSplitThreads, 3) kv_split_kernel(Params p) 
         const uint32_t g = c + k * kKvSplitThreads + tid;
         idx[k] = -2;
         if (g < total) {
-          uint32_t base = 0;
-          for (int q = 0; q < P; ++q) {
-            const int32_t* cq = p.seg_counts + ((int64_t)r * P + q) * 2;
-            const uint32_t n0 = (uint32_t)__ldcg(cq);
-            const uint32_t nb = with_band ? (uint32_t)__ldcg(cq + 1) : 0u;
-            if (g < base + n0 + nb) {
-              int slo, shi;
-              segment_bounds(L, P, q, slo, shi);
-              const uint32_t off = g - base;
-              // band entries occupy [shi - nb, shi); read them in ascending
-              // order so that every source position is >= its logical index
-              const int src = off < n0 ? slo + (int)off : shi - (int)nb + (int)(off - n0);
-              idx[k] = __ldcg(rb_idx + src);
-              key[k] = __ldcg(rb_key + src);
-              break;
-            }
-            base += n0 + nb;
+          int lo_q = 0, hi_q = P - 1;  // last q with run_pre[q] <= g
+          while (lo_q < hi_q) {
+            const int mid = (lo_q + hi_q + 1) >> 1;
+            if (st.run_pre[mid] <= g)
+              lo_q = mid;
+            else
+              hi_q = mid - 1;
           }
+          const int q = lo_q;
+          int slo, shi;
+          segment_bounds(L, P, q, slo, shi);
+          const uint32_t off = g - st.run_pre[q];
+          const uint32_t n0 = st.run_c0[q];
+          // band entries occupy [shi - nb, shi); read them in ascending order
+          // so that every source position is >= its logical position
+          const int src = off < n0 ? slo + (int)off
+                                   : shi - (int)st.run_cb[q] + (int)(off - n0);
+          const uint2 e = __ldcg(rb + src);
+          idx[k] = (int32_t)e.x;
+          key[k] = e.y;
         }
       }
       __syncthreads();
@@ -1031,8 +1462,10 @@ int set_attrs(KernelT kernel, int family, size_t smem) {
 }  // namespace
 
 size_t shared_bytes(int family, int cap) {
-  (void)family;
-  return sizeof(RowState) + (size_t)cap * (sizeof(int32_t) + sizeof(uint32_t));
+  const int threads =
+      family == EXACT_TOPK_FAMILY_ROW_LOCAL_EXACT ? kRowLocalThreads : kPersistentThreads;
+  return sizeof(RowState) + (size_t)cap * sizeof(uint2) +
+         (size_t)(threads / 32) * kQueueWords * sizeof(uint32_t);
 }
 
 int kernel_occupancy(int family, int device, int* ctas_per_sm) {
@@ -1088,13 +1521,8 @@ int launch(const exact_topk_plan& plan, const LaunchArgs& a, cudaStream_t stream
   p.num_valid_rows = a.num_valid_rows;
   p.counters = static_cast<int32_t*>(a.counters);
   unsigned char* ws = static_cast<unsigned char*>(a.workspace);
-  if (lay.slices > 0 && ws != nullptr) {
-    p.ws_idx = reinterpret_cast<int32_t*>(ws + lay.idx_offset);
-    p.ws_key = reinterpret_cast<uint32_t*>(ws + lay.key_offset);
-  } else {
-    p.ws_idx = nullptr;
-    p.ws_key = nullptr;
-  }
+  p.ws = (lay.slices > 0 && ws != nullptr) ? reinterpret_cast<uint2*>(ws + lay.pair_offset)
+                                            : nullptr;
   p.seg_counts = plan.family == EXACT_TOPK_FAMILY_KV_SPLIT
                      ? reinterpret_cast<int32_t*>(ws + lay.seg_offset)
                      : nullptr;
@@ -1109,6 +1537,7 @@ int launch(const exact_topk_plan& plan, const LaunchArgs& a, cudaStream_t stream
       persistent_sampled_kernel<<<plan.workers, kPersistentThreads, smem, stream>>>(p);
       break;
     case EXACT_TOPK_FAMILY_KV_SPLIT: {
+      if (plan.splits > kMaxSplits) return EXACT_TOPK_ERR_BAD_PLAN;
       rc = set_attrs(kv_split_kernel, EXACT_TOPK_FAMILY_KV_SPLIT, smem);
       if (rc != EXACT_TOPK_OK) return rc;
       const dim3 grid((unsigned)plan.splits, (unsigned)plan.num_rows);
@@ -1127,6 +1556,7 @@ int launch(const exact_topk_plan& plan, const LaunchArgs& a, cudaStream_t stream
 }
 
 }  // namespace etk
+
 
 // ----------------------------------------------------------------------------
 // Allocation-free entry point

@@ -114,7 +114,7 @@ typedef struct exact_topk_plan_request {
   int32_t family;        /* exact_topk_family */
   int32_t stride;        /* view stride s: power of two in [2, 4096] */
   int32_t dual;          /* -1 planner, 0 primary-only, 1 primary + secondary boundary */
-  int32_t splits;        /* KV-split segment count P in [1, 256] */
+  int32_t splits;        /* KV-split segment count P in [1, 128] */
   int32_t workers;       /* persistent / row-local grid size */
   int32_t rho0_num, rho0_den; /* primary retention margin rho (K~ = rho K), default 3/2 */
   int32_t rho1_num, rho1_den; /* secondary margin rho1, default 7/4 */
