@@ -86,15 +86,17 @@ _lib = None
 
 
 def library_path() -> str:
-    return _build.LIBRARY
+    return os.environ.get("EXACT_TOPK_LIBRARY") or _build.LIBRARY
 
 
 def library():
-    """Loads (building first if needed) libexact_topk.so; raises if impossible."""
+    """Loads libexact_topk.so (building it in-tree first if needed; the
+    EXACT_TOPK_LIBRARY environment variable names another build of the same
+    library to load instead); raises if impossible."""
     global _lib
     if _lib is not None:
         return _lib
-    path = _build.build()
+    path = os.environ.get("EXACT_TOPK_LIBRARY") or _build.build()
     if not os.path.exists(path):
         raise RuntimeError(f"exact_topk CUDA library missing: {path}")
     lib = ctypes.CDLL(path)

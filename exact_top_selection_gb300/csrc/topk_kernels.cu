@@ -27,9 +27,7 @@
 //
 // Complete-row passes stream the row with 256-bit loads that carry an L2
 // evict-first hint, so the lines the Phase-1 view touched (loaded with normal
-// priority) tend to stay in L2 until the complete-row pass reaches them.  Each
-// thread filters a tile of 16 scores with one max (or min) reduction; only
-// tiles holding a candidate take the warp-aggregated append path.
+// priority) tend to stay in L2 until the complete-row pass reaches them.
 
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -44,23 +42,27 @@ namespace {
 
 constexpr int kCoarseBins = 2048;
 constexpr int kMaxSplits = 128;
-// Resident CTAs per SM the sampled kernels are compiled for (register budget).
-#ifndef ETK_SAMPLED_MIN_CTAS
-#define ETK_SAMPLED_MIN_CTAS 2
+// Depth of each thread's ring of 256-bit loads in a complete-row pass.
+#ifndef ETK_RING
+#define ETK_RING 4
 #endif
-// 256-bit loads per thread per tile of a complete-row pass.
-#ifndef ETK_TILE_V8
-#define ETK_TILE_V8 2
-#endif
-// L2 eviction hint of complete-row loads: 1 = evict first, 0 = none.
-#ifndef ETK_L2_EVICT_FIRST
-#define ETK_L2_EVICT_FIRST 1
-#endif
-constexpr int kTileV8 = ETK_TILE_V8;
-constexpr int kTileScores = 8 * kTileV8;
+constexpr int kRing = ETK_RING;
 constexpr uint32_t kDescPosInf = 0x007FFFFFu;  // kappa_down32(+inf)
 constexpr uint32_t kDescNegInf = 0xFF800000u;  // kappa_down32(-inf)
 constexpr unsigned kFull = 0xFFFFFFFFu;
+
+// ----------------------------------------------------------------------------
+// Thread groups
+// ----------------------------------------------------------------------------
+
+// The whole CTA.
+template <int THREADS>
+struct CtaGroup {
+  static constexpr int kThreads = THREADS;
+  static constexpr int kWarps = THREADS / 32;
+  __device__ __forceinline__ static int rank() { return (int)threadIdx.x; }
+  __device__ __forceinline__ static void sync() { __syncthreads(); }
+};
 
 // ----------------------------------------------------------------------------
 // Keys and the coarse map
@@ -89,8 +91,8 @@ __device__ __forceinline__ int coarse_bin(uint32_t u) { return coarse_bin(u, des
 // endpoint of the admitted prefix (section 4.3; section 5.2 "converts the
 // selected bins to their inclusive FP32 endpoints").  c is non-decreasing along
 // the key space, so a search finds it; the 32 lanes of one warp test 32
-// evenly spaced keys per step, shrinking the interval ~33-fold.  Must be
-// called by all 32 lanes of a warp; every lane returns the result.
+// evenly spaced keys per step.  Must be called by all 32 lanes of a warp;
+// every lane returns the result.
 __device__ uint32_t cutoff_for_bin_warp(int tau) {
   const int lane = threadIdx.x & 31;
   uint32_t lo = 0u, hi = 0xFFFFFFFFu;  // c(lo) <= tau for tau >= 0; answer in [lo, hi]
@@ -114,9 +116,60 @@ __device__ uint32_t cutoff_for_bin_warp(int tau) {
   return lo;
 }
 
+// Closed-form candidate for cutoff_for_bin: bin tau's smallest admitted half
+// is the one with kappa_down16 = 32 tau + 31; an FP32 score rounds (to nearest,
+// ties to even) to that half or above iff it is >= the midpoint between the
+// half and its lower neighbour (the midpoint itself when the half's mantissa
+// is even, the next FP32 value above it otherwise).  Returns the key of that
+// smallest admitted score; callers verify it.
+__device__ __forceinline__ uint32_t cutoff_candidate(int tau) {
+  if (tau >= kCoarseBins - 1) return 0xFFFFFFFFu;
+  if (tau >= (int)(0xFC00u >> 5)) return kDescNegInf;  // c(-inf): every number admitted
+  const uint32_t D = 32u * (uint32_t)tau + 31u;
+  const uint32_t h = (D & 0x8000u) ? D : (D ^ 0x7FFFu);
+  if (h == 0x0000u) return desc_key(0u);  // +0: every non-negative score
+  float mid;
+  if (h == 0x7C00u) {
+    mid = 65520.0f;  // between 65504 and +inf
+  } else if (h == 0xFBFFu) {
+    mid = -65520.0f;  // between -65504 and -inf
+  } else {
+    const uint32_t hlo = (h & 0x8000u) ? h + 1u : h - 1u;  // next smaller half
+    const float v = __half2float(__ushort_as_half((unsigned short)h));
+    const float vlo = __half2float(__ushort_as_half((unsigned short)hlo));
+    mid = (v + vlo) * 0.5f;  // exact: both are halves
+  }
+  uint32_t m = __float_as_uint(mid);
+  if (h & 1u) m = (m & 0x80000000u) ? m - 1u : m + 1u;  // odd half: ties go below
+  return desc_key(m);
+}
+
+// Cutoff of bin tau for one thread: the closed-form candidate when it
+// verifies as the largest key with c <= tau, else the warp search's answer
+// (the warp-wide form is used by callers that hold a whole warp).
+__device__ __forceinline__ bool cutoff_verified(int tau, uint32_t T) {
+  if (coarse_bin(bits_from_desc(T), T) > tau) return false;
+  if (T == 0xFFFFFFFFu) return true;
+  return coarse_bin(bits_from_desc(T + 1u), T + 1u) > tau;
+}
+
+// Warp-wide cutoff: candidate first, search only if it does not verify.
+__device__ __forceinline__ uint32_t cutoff_fast_warp(int tau) {
+  const uint32_t T = cutoff_candidate(tau);
+  const bool ok = tau >= 0 && cutoff_verified(tau, T);
+  if (__all_sync(kFull, ok)) return T;
+  return cutoff_for_bin_warp(tau);
+}
+
 // Digit j of the 11+11+10 split, most significant first (section 4.3).
 __device__ __forceinline__ uint32_t digit(uint32_t d, int j) {
   return j == 0 ? (d >> 21) : (j == 1 ? ((d >> 10) & 0x7FFu) : (d & 0x3FFu));
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
 }
 
 // ----------------------------------------------------------------------------
@@ -126,17 +179,10 @@ __device__ __forceinline__ uint32_t digit(uint32_t d, int j) {
 // 256-bit streaming load of 8 score bit patterns (32-byte aligned address),
 // read once per complete-row pass: no L1 allocation, evict first from L2.
 __device__ __forceinline__ void ld_stream8(const float* p, uint32_t* x) {
-#if ETK_L2_EVICT_FIRST
   asm("ld.global.nc.L1::no_allocate.L2::evict_first.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
       : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]), "=r"(x[4]), "=r"(x[5]), "=r"(x[6]),
         "=r"(x[7])
       : "l"(p));
-#else
-  asm("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-      : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]), "=r"(x[4]), "=r"(x[5]), "=r"(x[6]),
-        "=r"(x[7])
-      : "l"(p));
-#endif
 }
 
 __device__ __forceinline__ uint32_t ld_stream1(const float* p) {
@@ -145,33 +191,50 @@ __device__ __forceinline__ uint32_t ld_stream1(const float* p) {
   return v;
 }
 
+// Asynchronous 4-byte copy global -> shared (cp.async); completion is awaited
+// with cp_async_wait_all by the issuing thread.
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
+  const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // ----------------------------------------------------------------------------
-// Per-CTA shared state
+// Shared state
 // ----------------------------------------------------------------------------
 
-struct alignas(16) RowState {
-  uint32_t hist[kCoarseBins];   // h_{r,s} -> h0 (Fig. 5); refinement alternates with hist2
-  uint32_t hist2[kCoarseBins];
+// Scratch of one thread group for block-wide scans and boundary search.
+struct GroupScratch {
   uint32_t warp_sums[32];
-  uint32_t run_pre[kMaxSplits + 1];  // KV-split finisher: run prefix over segments
-  uint32_t run_c0[kMaxSplits];       // KV-split finisher: primary count per segment
-  uint32_t run_cb[kMaxSplits];       // KV-split finisher: band count per segment
   int32_t res_bin[2];
   uint32_t res_below[2];
   uint32_t res_cnt[2];
+  int32_t gmax;      // guess source: worst coarse bin
+  int32_t ginvalid;  // guess source: an entry outside [0, L)
+  int32_t bcast;     // broadcast word
+  int32_t pad_;
+};
+
+// One row in flight: its proposal, counters and route record.
+struct Slot {
+  int32_t row;  // -1: no more rows
+  int32_t L;
+  int32_t route;
+  uint32_t T0, T1;  // kappa_down32 cutoffs
+  int32_t tau0, tau1;
   uint32_t n_front;  // frontier entries
   uint32_t n_out;    // output slots used
   uint32_t n_keep;   // survivors during an in-place compaction
   uint32_t n_drop;   // sink for counts that are not kept
-  uint32_t cut[2];   // kappa_down32 cutoffs
-  int32_t gmax;      // guess source: worst coarse bin
-  int32_t ginvalid;  // guess source: an entry outside [0, L)
-  int32_t next_row;
+  int32_t c0, c1, tstar, e0, q0n;
+  uint32_t seg_c0, seg_cb;  // KV-split: this segment's counts
   int32_t is_last;
-  uint32_t seg_c0;   // KV-split: this segment's primary candidates
-  uint32_t seg_cb;   // KV-split: this segment's band candidates
-  uint32_t tot_c0;   // KV-split finisher: merged counts
-  uint32_t tot_cb;
+  int32_t pf_row;  // persistent: row whose view sits in the prefetch buffer, or -1
+  int32_t pf_n;    // number of prefetched view entries
+  int32_t pad_[1];
 };
 
 struct Params {
@@ -200,8 +263,8 @@ struct Params {
 // Candidate frontier: logical entries [0, cap) live in shared memory, entries
 // at logical positions >= cap live at the same position of a global slice of
 // capacity gcap (section 5.4: "Two global ping-pong slices extend the shared
-// frontier"; here one slice suffices because compaction is done in place).
-// Entries are (index, key) pairs stored together.
+// frontier"; here one slice per row slot suffices because compaction is done
+// in place).  Entries are (index, key) pairs stored together.
 struct Frontier {
   uint2* s;
   uint32_t cap;
@@ -225,48 +288,93 @@ struct Frontier {
   }
 };
 
-// Dynamic shared memory: RowState, then cap frontier pairs, then one
-// candidate-vector stack per warp.
-__device__ __forceinline__ uint32_t* queue_area(const Params& p) {
+// Per-warp stack of 8-score vectors that hold at least one admitted score:
+// kQueueCap entries of 8 bit patterns plus the vector's index in the pass.
+constexpr int kQueueCap = 64;  // < 32 before a vector slot + at most 32 pushed by it
+constexpr int kQueueWords = kQueueCap * 9;
+// View entries of the next row prefetched into shared memory (persistent kernel).
+constexpr int kViewPrefetch = 4096;
+
+// Dynamic shared memory layouts (byte offsets), one per kernel family.
+struct SmemLayout {
+  uint32_t slots;     // Slot[nslots]
+  uint32_t scratch;   // GroupScratch[2]
+  uint32_t hist;      // uint32[nslots][2048]
+  uint32_t frontier;  // uint2[nslots][cap]
+  uint32_t runs;      // KV-split run table, or 0
+  uint32_t view;      // persistent: prefetched view of the next row, or 0
+  uint32_t queues;    // uint32[warps][kQueueWords]
+  uint32_t total;
+};
+
+__host__ __device__ constexpr uint32_t align16(uint32_t v) { return (v + 15u) & ~15u; }
+
+__host__ __device__ inline SmemLayout smem_layout(int family, int cap) {
+  SmemLayout l{};
+  const bool pers = family == EXACT_TOPK_FAMILY_PERSISTENT_SAMPLED;
+  const int nslots = 1;
+  const int qwarps = pers ? kPersistentThreads / 32
+                          : (family == EXACT_TOPK_FAMILY_KV_SPLIT ? kKvSplitThreads / 32
+                                                                  : kRowLocalThreads / 32);
+  uint32_t o = 0;
+  l.slots = o;
+  o = align16(o + nslots * (uint32_t)sizeof(Slot));
+  l.scratch = o;
+  o = align16(o + 2 * (uint32_t)sizeof(GroupScratch));
+  l.hist = o;
+  o = align16(o + nslots * kCoarseBins * 4u);
+  l.frontier = o;
+  o = align16(o + nslots * (uint32_t)cap * 8u);
+  l.runs = family == EXACT_TOPK_FAMILY_KV_SPLIT ? o : 0u;
+  if (family == EXACT_TOPK_FAMILY_KV_SPLIT) o = align16(o + (3 * kMaxSplits + 1) * 4u);
+  l.view = pers ? o : 0u;
+  if (pers) o = align16(o + kViewPrefetch * 4u);
+  l.queues = o;
+  o = align16(o + qwarps * kQueueWords * 4u);
+  l.total = o;
+  return l;
+}
+
+__device__ __forceinline__ unsigned char* smem_base() {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  return reinterpret_cast<uint32_t*>(smem_raw + sizeof(RowState) + sizeof(uint2) * (size_t)p.cap);
+  return smem_raw;
 }
 
 __device__ __forceinline__ void flag_status(int32_t* counters, int bit) {
   atomicOr(counters + kCtrStatus, bit);
 }
 
-template <int THREADS>
-__device__ __forceinline__ void clear_hist(RowState& st, int nbins) {
-  for (int b = threadIdx.x; b < nbins; b += THREADS) st.hist[b] = 0u;
+template <class G>
+__device__ __forceinline__ void clear_hist(uint32_t* hist, int nbins) {
+  for (int b = G::rank(); b < nbins; b += G::kThreads) hist[b] = 0u;
 }
 
 // For each target t (ntargets <= 2): res_bin = min{b : H(b) >= t} over the
 // inclusive prefix H of hist[0, nbins), res_below = H(b - 1) and res_cnt =
 // hist[b]; res_bin = -1 (res_below = total) when the total is below t.  The
-// histogram is only read.  Must be entered by the whole CTA after the
-// histogram is complete, with a barrier between consecutive calls (results of
-// a call are written exactly once, by the thread owning the boundary bin or
-// by the last thread); results are visible to every thread on return.
-template <int THREADS>
-__device__ void find_boundaries_in(const uint32_t* hist, RowState& st, int nbins, int ntargets,
-                                   uint32_t t0, uint32_t t1) {
-  constexpr int kWarps = THREADS / 32;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int per = nbins / THREADS;  // nbins is 1024 or 2048, THREADS 512 or 1024
+// histogram is only read.  Entered by the whole group after the histogram is
+// complete, with a group barrier between consecutive calls (results of a call
+// are written exactly once, by the thread owning the boundary bin or by the
+// last thread); results are visible to every thread of the group on return.
+template <class G>
+__device__ void find_boundaries(const uint32_t* hist, GroupScratch& sc, int nbins, int ntargets,
+                                uint32_t t0, uint32_t t1) {
+  constexpr int kWarps = G::kWarps;
+  const int tid = G::rank(), lane = tid & 31, warp = tid >> 5;
+  const int per = (nbins + G::kThreads - 1) / G::kThreads;
   const int b0 = tid * per;
   uint32_t local = 0;
-  for (int k = 0; k < per; ++k) local += hist[b0 + k];
+  for (int k = 0; k < per; ++k) local += b0 + k < nbins ? hist[b0 + k] : 0u;
   uint32_t incl = local;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const uint32_t v = __shfl_up_sync(kFull, incl, o);
     if (lane >= o) incl += v;
   }
-  if (lane == 31) st.warp_sums[warp] = incl;
-  __syncthreads();
+  if (lane == 31) sc.warp_sums[warp] = incl;
+  G::sync();
   // Every warp scans the warp totals itself (no second barrier).
-  uint32_t w = lane < kWarps ? st.warp_sums[lane] : 0u;
+  uint32_t w = lane < kWarps ? sc.warp_sums[lane] : 0u;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const uint32_t v = __shfl_up_sync(kFull, w, o);
@@ -276,39 +384,33 @@ __device__ void find_boundaries_in(const uint32_t* hist, RowState& st, int nbins
   const uint32_t grand = __shfl_sync(kFull, w, kWarps - 1);
   uint32_t run = before_warp + (incl - local);
   for (int k = 0; k < per; ++k) {
-    const uint32_t h = hist[b0 + k];
+    const uint32_t h = b0 + k < nbins ? hist[b0 + k] : 0u;
     const uint32_t prev = run;
     run += h;
     if (prev < t0 && t0 <= run) {
-      st.res_bin[0] = b0 + k;
-      st.res_below[0] = prev;
-      st.res_cnt[0] = h;
+      sc.res_bin[0] = b0 + k;
+      sc.res_below[0] = prev;
+      sc.res_cnt[0] = h;
     }
     if (ntargets > 1 && prev < t1 && t1 <= run) {
-      st.res_bin[1] = b0 + k;
-      st.res_below[1] = prev;
-      st.res_cnt[1] = h;
+      sc.res_bin[1] = b0 + k;
+      sc.res_below[1] = prev;
+      sc.res_cnt[1] = h;
     }
   }
-  if (tid == THREADS - 1) {
+  if (tid == G::kThreads - 1) {
     if (grand < t0) {
-      st.res_bin[0] = -1;
-      st.res_below[0] = grand;
-      st.res_cnt[0] = 0u;
+      sc.res_bin[0] = -1;
+      sc.res_below[0] = grand;
+      sc.res_cnt[0] = 0u;
     }
     if (ntargets > 1 && grand < t1) {
-      st.res_bin[1] = -1;
-      st.res_below[1] = grand;
-      st.res_cnt[1] = 0u;
+      sc.res_bin[1] = -1;
+      sc.res_below[1] = grand;
+      sc.res_cnt[1] = 0u;
     }
   }
-  __syncthreads();
-}
-
-template <int THREADS>
-__device__ __forceinline__ void find_boundaries(RowState& st, int nbins, int ntargets, uint32_t t0,
-                                                uint32_t t1) {
-  find_boundaries_in<THREADS>(st.hist, st, nbins, ntargets, t0, t1);
+  G::sync();
 }
 
 // ----------------------------------------------------------------------------
@@ -335,44 +437,20 @@ __device__ __forceinline__ Span aligned_span(const float* row, int lo, int hi) {
   return s;
 }
 
-__device__ __forceinline__ uint32_t lanemask_lt() {
-  uint32_t m;
-  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-  return m;
-}
-
-// Per-warp stack of 8-score vectors that hold at least one admitted score:
-// kQueueCap entries of 8 bit patterns plus the vector's index in the pass.
-constexpr int kQueueCap = 32 + 32 * kTileV8;  // < 32 before a tile + one tile's pushes
-constexpr int kQueueWords = kQueueCap * 9;
-
 struct WarpQueue {
   uint32_t* vals;  // [kQueueCap][8]
   int32_t* vidx;   // [kQueueCap]
 };
 
-// One pass over row[lo, hi) that classifies every score by its key d into
-//   class A: d <= TA            (only when A_ON)
-//   class B: d <= TB otherwise  (TB >= TA)
-// and hands each admitted (position, index, key) to sinkA / sinkB, where the
-// position comes from the shared counter cntA / cntB.
-//
-// Streaming part, per thread: tiles of kTileV8 256-bit vectors, the next
-// tile's loads issued before the current tile is filtered.  A vector is kept
-// when its largest score passes (SIGNED_FAST: the cutoff TB is a non-negative
-// score, so "d <= TB" is the signed compare (int)u >= (int)bits(TB) on the raw
-// bits); one ballot per vector slot pushes the kept vectors onto the warp's
-// stack.  Candidate part, per warp: whenever 32 vectors are stacked, each lane
-// takes one, forms its admission mask, and the warp reserves positions with a
-// scan and one shared atomic per class.  Candidate work therefore runs with
-// full lanes instead of one lane per candidate.
-template <int THREADS, bool SIGNED_FAST, bool A_ON, class SinkA, class SinkB>
+// Processes the top min(n, 32) stacked vectors: each lane takes one, forms
+// its admission masks, and the warp reserves positions with a scan and one
+// shared atomic per class.
+template <bool SIGNED_FAST, bool A_ON, class SinkA, class SinkB>
 __device__ __forceinline__ void drain_queue(const WarpQueue& q, int n, int a0, int CA, int CB,
                                             uint32_t TA, uint32_t TB, uint32_t* cntA,
                                             uint32_t* cntB, const SinkA& sinkA,
                                             const SinkB& sinkB) {
   const int lane = threadIdx.x & 31;
-  const uint32_t lt = lanemask_lt();
   const int j = n - 32 + lane;  // n >= 32, or a final partial drain with n < 32
   const bool act = j >= 0;
   uint32_t u[8];
@@ -380,8 +458,14 @@ __device__ __forceinline__ void drain_queue(const WarpQueue& q, int n, int a0, i
   if (act) {
     const uint4 v0 = *reinterpret_cast<const uint4*>(q.vals + 8 * j);
     const uint4 v1 = *reinterpret_cast<const uint4*>(q.vals + 8 * j + 4);
-    u[0] = v0.x; u[1] = v0.y; u[2] = v0.z; u[3] = v0.w;
-    u[4] = v1.x; u[5] = v1.y; u[6] = v1.z; u[7] = v1.w;
+    u[0] = v0.x;
+    u[1] = v0.y;
+    u[2] = v0.z;
+    u[3] = v0.w;
+    u[4] = v1.x;
+    u[5] = v1.y;
+    u[6] = v1.z;
+    u[7] = v1.w;
     vi = q.vidx[j];
   } else {
 #pragma unroll
@@ -415,7 +499,6 @@ __device__ __forceinline__ void drain_queue(const WarpQueue& q, int n, int a0, i
   bB = __shfl_sync(kFull, bB, 0);
   const uint32_t excl = incl - packed;
   uint32_t pA = bA + (excl & 0xFFFFu), pB = bB + (excl >> 16);
-  (void)lt;
   const int ibase = a0 + 8 * vi;
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
@@ -429,13 +512,28 @@ __device__ __forceinline__ void drain_queue(const WarpQueue& q, int n, int a0, i
   }
 }
 
-template <int THREADS, bool SIGNED_FAST, bool A_ON, class SinkA, class SinkB>
+// One pass of group G over row[lo, hi) that classifies every score by its
+// key d into
+//   class A: d <= TA            (only when A_ON)
+//   class B: d <= TB otherwise  (TB >= TA)
+// and hands each admitted (position, index, key) to sinkA / sinkB, where the
+// position comes from the shared counter cntA / cntB.  No group barrier.
+//
+// Streaming part, per thread: a ring of kRing 256-bit vectors, kRing - 1 of
+// them in flight while one is filtered.  A vector is kept
+// when its largest score passes (SIGNED_FAST: the cutoff TB is a non-negative
+// score, so "d <= TB" is the signed compare (int)u >= (int)bits(TB) on the raw
+// bits); one ballot per vector slot pushes the kept vectors onto the warp's
+// stack.  Candidate part, per warp: whenever 32 vectors are stacked, each
+// lane takes one, so candidate work runs with full lanes instead of one lane
+// per candidate.
+template <class G, bool SIGNED_FAST, bool A_ON, class SinkA, class SinkB>
 __device__ __forceinline__ void scan_tiles(const float* row, int lo, int hi, uint32_t TA,
                                            uint32_t TB, uint32_t* cntA, uint32_t* cntB,
                                            uint32_t* queues, const SinkA& sinkA,
                                            const SinkB& sinkB) {
   if (lo >= hi) return;
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = G::rank();
   const Span sp = aligned_span(row, lo, hi);
   const int head = sp.a0 - lo, tail = hi - sp.a_end;
   if (tid < head + tail) {
@@ -456,82 +554,81 @@ __device__ __forceinline__ void scan_tiles(const float* row, int lo, int hi, uin
   q.vidx = reinterpret_cast<int32_t*>(q.vals + kQueueCap * 8);
   int qn = 0;  // warp-uniform stack depth
   const float* body = row + sp.a0;
-  constexpr int kStep = kTileV8 * THREADS;
   constexpr uint32_t kSentinel = SIGNED_FAST ? 0x80000000u : 0xFFFFFFFFu;
-  uint32_t x[kTileScores];
+  // Ring of kRing single-vector tiles: tile k of this thread is the vector
+  // k * kThreads + rank; while tile k is filtered, tiles k+1 .. k+kRing-1 are
+  // in flight.  Slot indices are compile-time (the ring is unrolled).
+  const int ntiles = (sp.nvec + G::kThreads - 1) / G::kThreads;
+  uint32_t buf[kRing][8];
 #pragma unroll
-  for (int g = 0; g < kTileV8; ++g) {
-    const int idx = g * THREADS + tid;
-    if (idx < sp.nvec) {
-      ld_stream8(body + 8 * idx, &x[8 * g]);
+  for (int u = 0; u < kRing - 1; ++u) {
+    const int vi = u * G::kThreads + tid;
+    if (vi < sp.nvec) {
+      ld_stream8(body + 8 * vi, buf[u]);
     } else {
 #pragma unroll
-      for (int k = 0; k < 8; ++k) x[8 * g + k] = kSentinel;
+      for (int e = 0; e < 8; ++e) buf[u][e] = kSentinel;
     }
   }
-  for (int t = 0; t < sp.nvec; t += kStep) {
-    uint32_t y[kTileScores];
-    const bool more = t + kStep < sp.nvec;
+  for (int base = 0; base < ntiles; base += kRing) {
 #pragma unroll
-    for (int g = 0; g < kTileV8; ++g) {
-      const int idx = t + kStep + g * THREADS + tid;
-      if (more && idx < sp.nvec) {
-        ld_stream8(body + 8 * idx, &y[8 * g]);
-      } else {
+    for (int u = 0; u < kRing; ++u) {
+      const int k = base + u;
+      if (k >= ntiles) break;
+      {
+        constexpr int kAhead = kRing - 1;
+        const int vp = (k + kAhead) * G::kThreads + tid;
+        uint32_t* dst = buf[(u + kAhead) % kRing];
+        if (vp < sp.nvec) {
+          ld_stream8(body + 8 * vp, dst);
+        } else {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) y[8 * g + k] = kSentinel;
+          for (int e = 0; e < 8; ++e) dst[e] = kSentinel;
+        }
       }
-    }
-#pragma unroll
-    for (int g = 0; g < kTileV8; ++g) {
-      const int vi = t + g * THREADS + tid;
+      const uint32_t* x = buf[u];
+      const int vi = k * G::kThreads + tid;
       bool keep;
       if (SIGNED_FAST) {
-        int mx = (int)x[8 * g];
+        int mx = (int)x[0];
 #pragma unroll
-        for (int k = 1; k < 8; ++k) mx = max(mx, (int)x[8 * g + k]);
-        keep = mx >= CB;
+        for (int e = 1; e < 8; ++e) mx = max(mx, (int)x[e]);
+        keep = mx >= CB;  // the sentinel is never admitted
       } else {
-        uint32_t mn = desc_key(x[8 * g]);
+        uint32_t mn = desc_key(x[0]);
 #pragma unroll
-        for (int k = 1; k < 8; ++k) mn = min(mn, desc_key(x[8 * g + k]));
+        for (int e = 1; e < 8; ++e) mn = min(mn, desc_key(x[e]));
         keep = vi < sp.nvec && mn <= TB;
       }
       const uint32_t bal = __ballot_sync(kFull, keep);
       if (bal != 0u) {
         if (keep) {
           const int pos = qn + __popc(bal & lt);
-          uint4* dst = reinterpret_cast<uint4*>(q.vals + 8 * pos);
-          dst[0] = make_uint4(x[8 * g], x[8 * g + 1], x[8 * g + 2], x[8 * g + 3]);
-          dst[1] = make_uint4(x[8 * g + 4], x[8 * g + 5], x[8 * g + 6], x[8 * g + 7]);
+          uint4* qdst = reinterpret_cast<uint4*>(q.vals + 8 * pos);
+          qdst[0] = make_uint4(x[0], x[1], x[2], x[3]);
+          qdst[1] = make_uint4(x[4], x[5], x[6], x[7]);
           q.vidx[pos] = vi;
         }
         qn += __popc(bal);
+        if (qn >= 32) {
+          __syncwarp();
+          drain_queue<SIGNED_FAST, A_ON>(q, qn, sp.a0, CA, CB, TA, TB, cntA, cntB, sinkA, sinkB);
+          qn -= 32;
+          __syncwarp();
+        }
       }
     }
-    if (qn >= 32) {
-      __syncwarp();
-      do {
-        drain_queue<THREADS, SIGNED_FAST, A_ON>(q, qn, sp.a0, CA, CB, TA, TB, cntA, cntB, sinkA,
-                                                sinkB);
-        qn -= 32;
-      } while (qn >= 32);
-      __syncwarp();
-    }
-#pragma unroll
-    for (int k = 0; k < kTileScores; ++k) x[k] = y[k];
   }
   if (qn > 0) {
     __syncwarp();
-    drain_queue<THREADS, SIGNED_FAST, A_ON>(q, qn, sp.a0, CA, CB, TA, TB, cntA, cntB, sinkA,
-                                            sinkB);
+    drain_queue<SIGNED_FAST, A_ON>(q, qn, sp.a0, CA, CB, TA, TB, cntA, cntB, sinkA, sinkB);
     __syncwarp();
   }
 }
 
 // Dispatches on the cutoff's sign (signed-compare fast path) and on whether
 // class A exists.
-template <int THREADS, class SinkA, class SinkB>
+template <class G, class SinkA, class SinkB>
 __device__ __forceinline__ void scan_two_class(const float* row, int lo, int hi, uint32_t TA,
                                                uint32_t TB, bool a_on, uint32_t* cntA,
                                                uint32_t* cntB, uint32_t* queues,
@@ -539,39 +636,40 @@ __device__ __forceinline__ void scan_two_class(const float* row, int lo, int hi,
   const bool fast = (bits_from_desc(TB) & 0x80000000u) == 0u;
   if (fast) {
     if (a_on)
-      scan_tiles<THREADS, true, true>(row, lo, hi, TA, TB, cntA, cntB, queues, sinkA, sinkB);
+      scan_tiles<G, true, true>(row, lo, hi, TA, TB, cntA, cntB, queues, sinkA, sinkB);
     else
-      scan_tiles<THREADS, true, false>(row, lo, hi, TA, TB, cntA, cntB, queues, sinkA, sinkB);
+      scan_tiles<G, true, false>(row, lo, hi, TA, TB, cntA, cntB, queues, sinkA, sinkB);
   } else {
     if (a_on)
-      scan_tiles<THREADS, false, true>(row, lo, hi, TA, TB, cntA, cntB, queues, sinkA, sinkB);
+      scan_tiles<G, false, true>(row, lo, hi, TA, TB, cntA, cntB, queues, sinkA, sinkB);
     else
-      scan_tiles<THREADS, false, false>(row, lo, hi, TA, TB, cntA, cntB, queues, sinkA, sinkB);
+      scan_tiles<G, false, false>(row, lo, hi, TA, TB, cntA, cntB, queues, sinkA, sinkB);
   }
 }
 
-// Coarse histogram over row[lo, hi) (first pass of exact coarse recovery, eq. 20).
-template <int THREADS>
-__device__ void scan_coarse_hist(const float* row, int lo, int hi, RowState& st) {
+// Coarse histogram over row[lo, hi) by group G (first pass of exact coarse
+// recovery, eq. 20).  No group barrier.
+template <class G>
+__device__ void scan_coarse_hist(const float* row, int lo, int hi, uint32_t* hist) {
   if (lo >= hi) return;
-  const int tid = threadIdx.x;
+  const int tid = G::rank();
   const Span sp = aligned_span(row, lo, hi);
   const int head = sp.a0 - lo, tail = hi - sp.a_end;
   if (tid < head + tail) {
     const int i = tid < head ? lo + tid : sp.a_end + (tid - head);
-    atomicAdd(&st.hist[coarse_bin(ld_stream1(row + i))], 1u);
+    atomicAdd(&hist[coarse_bin(ld_stream1(row + i))], 1u);
   }
   const float* body = row + sp.a0;
-  for (int t = tid; t < sp.nvec; t += 2 * THREADS) {
+  for (int t = tid; t < sp.nvec; t += 2 * G::kThreads) {
     uint32_t x[16];
-    const bool second = t + THREADS < sp.nvec;
+    const bool second = t + G::kThreads < sp.nvec;
     ld_stream8(body + 8 * t, x);
-    if (second) ld_stream8(body + 8 * (t + THREADS), x + 8);
+    if (second) ld_stream8(body + 8 * (t + G::kThreads), x + 8);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) atomicAdd(&st.hist[coarse_bin(x[k])], 1u);
+    for (int k = 0; k < 8; ++k) atomicAdd(&hist[coarse_bin(x[k])], 1u);
     if (second) {
 #pragma unroll
-      for (int k = 8; k < 16; ++k) atomicAdd(&st.hist[coarse_bin(x[k])], 1u);
+      for (int k = 8; k < 16; ++k) atomicAdd(&hist[coarse_bin(x[k])], 1u);
     }
   }
 }
@@ -596,118 +694,13 @@ struct DropSink {
   __device__ __forceinline__ void operator()(uint32_t, int32_t, uint32_t) const {}
 };
 
-// Output slot reservation for one committed index.
-__device__ __forceinline__ void commit(RowState& st, int32_t* out_row, int K, int32_t i) {
-  const uint32_t slot = atomicAdd(&st.n_out, 1u);
-  if (slot < (uint32_t)K) out_row[slot] = i;
-}
-
-// ----------------------------------------------------------------------------
-// Phase 3: prefix-commit-retain refinement (section 4.4, eqs. 22-25)
-// ----------------------------------------------------------------------------
-
-// General form for frontiers that spill to global memory: in-place chunked
-// compaction of the frontier at every digit.
-// Entry: frontier holds n entries (Q0), st.hist holds h0 (digit 0 over Q0),
-// k = k0 indices remain to be selected, st.n_out = |E0|.  Exit: st.n_out == K.
-template <int THREADS>
-__device__ void refine_general(const Frontier& F, uint32_t n, uint32_t k, RowState& st,
-                               int32_t* out_row, int K) {
-  constexpr int R = 4;
-  constexpr uint32_t CH = THREADS * R;
-  const int tid = threadIdx.x;
-  for (int j = 0; j < 3 && k > 0; ++j) {
-    const int nb = (j == 2) ? 1024 : 2048;
-    find_boundaries<THREADS>(st, nb, 1, k, 0u);
-    const int b = st.res_bin[0];
-    const uint32_t below = st.res_below[0];
-    const uint32_t cnt = st.res_cnt[0];
-    if (b < 0) {  // inconsistent counts: cannot happen; finish_row flags it
-      k = 0;
-      break;
-    }
-    if (below + cnt == k) {
-      // The boundary group completes the quota exactly: commit every entry
-      // whose digit is <= b and stop.
-      for (uint32_t p = tid; p < n; p += THREADS) {
-        int32_t i;
-        uint32_t d;
-        F.get(p, i, d);
-        if ((int)digit(d, j) <= b) commit(st, out_row, K, i);
-      }
-      k = 0;
-      break;
-    }
-    __syncthreads();  // every thread has read res_* before hist is cleared
-    const bool next = j < 2;
-    if (next) clear_hist<THREADS>(st, 2048);
-    if (tid == 0) st.n_keep = 0u;
-    __syncthreads();
-    if (below == 0u && cnt == n) {
-      // Whole frontier in the boundary group: nothing to commit or move;
-      // only the next digit's histogram is needed.
-      if (next) {
-        for (uint32_t p = tid; p < n; p += THREADS) {
-          int32_t i;
-          uint32_t d;
-          F.get(p, i, d);
-          atomicAdd(&st.hist[digit(d, j + 1)], 1u);
-        }
-      }
-    } else {
-      // In-place compaction in chunks: every entry of a chunk is read before
-      // any survivor of that chunk is written, and survivors land at
-      // positions below the chunk's end, so no unread entry is overwritten.
-      for (uint32_t c0 = 0; c0 < n; c0 += CH) {
-        int32_t idx[R];
-        uint32_t key[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const uint32_t p = c0 + r * THREADS + tid;
-          if (p < n)
-            F.get(p, idx[r], key[r]);
-          else
-            idx[r] = -2;
-        }
-        __syncthreads();
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          if (idx[r] == -2) continue;
-          const int dg = (int)digit(key[r], j);
-          if (dg < b) {
-            commit(st, out_row, K, idx[r]);
-          } else if (dg == b) {
-            const uint32_t q = atomicAdd(&st.n_keep, 1u);
-            F.put(q, idx[r], key[r]);
-            if (next) atomicAdd(&st.hist[digit(key[r], j + 1)], 1u);
-          }
-        }
-        __syncthreads();
-      }
-      n = cnt;
-      k -= below;
-    }
-    __syncthreads();
-  }
-  if (k > 0) {
-    // After the last digit every remaining key is identical: fill from it.
-    for (uint32_t p = tid; p < k && p < n; p += THREADS) {
-      int32_t i;
-      uint32_t d;
-      F.get(p, i, d);
-      commit(st, out_row, K, i);
-    }
-  }
-  __syncthreads();
-}
-
 // Warp-aggregated commit of idx for the lanes where `com` holds.
-__device__ __forceinline__ void commit_warp(RowState& st, int32_t* out_row, int K, bool com,
+__device__ __forceinline__ void commit_warp(uint32_t* n_out, int32_t* out_row, int K, bool com,
                                             int32_t idx, uint32_t lt) {
   const uint32_t bal = __ballot_sync(kFull, com);
   if (bal == 0u) return;
   uint32_t base = 0u;
-  if ((threadIdx.x & 31) == 0) base = atomicAdd(&st.n_out, (uint32_t)__popc(bal));
+  if ((threadIdx.x & 31) == 0) base = atomicAdd(n_out, (uint32_t)__popc(bal));
   base = __shfl_sync(kFull, base, 0);
   if (com) {
     const uint32_t slot = base + (uint32_t)__popc(bal & lt);
@@ -715,116 +708,107 @@ __device__ __forceinline__ void commit_warp(RowState& st, int32_t* out_row, int 
   }
 }
 
-// Phase 3 (section 4.4, eqs. 22-25) with the frontier resident in registers:
-// each thread holds up to 8 (index, key) entries, so no entry moves between
-// digits; the histogram of the next digit is built in a second buffer while
-// the current digit is classified.  Same entry and exit conditions as
-// refine_general, to which frontiers beyond shared memory are handed.
-template <int THREADS>
-__device__ void refine(const Frontier& F, uint32_t n, uint32_t k, RowState& st, int32_t* out_row,
-                       int K) {
-  constexpr int EPT = 8;
-  if (n > F.cap || F.cap > (uint32_t)(EPT * THREADS)) {
-    refine_general<THREADS>(F, n, k, st, out_row, K);
-    return;
-  }
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+// ----------------------------------------------------------------------------
+// Phase 3: prefix-commit-retain refinement (section 4.4, eqs. 22-25)
+// ----------------------------------------------------------------------------
+
+// Phase 3 (eqs. 22-25) with the commits of every digit deferred to one final
+// pass.  Round j only needs h_j over the frontier entries whose leading digits
+// match b_0..b_{j-1} (Q_j) to find b_j = min{b : H_j(b) >= k_j} and k_{j+1} =
+// k_j - H_j(b_j - 1); the union of the groups R_j committed per round is
+// exactly {key < T*} with T* the key spelled by (b_0, b_1, b_2), and Q_3 is
+// {key == T*}, from which k_3 entries fill the rest.  When H_j(b_j) == k_j the
+// boundary group closes the quota at round j and no tie fill is needed.  The
+// frontier is only read (shared memory or its global slice), never moved.
+// Entry: frontier holds n entries (Q0), hist holds h0, k = k0 indices remain,
+// sl.n_out = |E0|.  Exit: sl.n_out == K.
+template <class G>
+__device__ void refine(const Frontier& F, uint32_t n, uint32_t k, uint32_t* hist,
+                       GroupScratch& sc, Slot& sl, int32_t* out_row, int K) {
+  const int tid = G::rank();
   const uint32_t lt = lanemask_lt();
-  uint32_t key[EPT];
-  int32_t idx[EPT];
-  uint32_t alive = 0u;
-#pragma unroll
-  for (int e = 0; e < EPT; ++e) {
-    const uint32_t p = (uint32_t)(e * THREADS + tid);
-    if (p < n) {
-      const uint2 v = F.s[p];
-      idx[e] = (int32_t)v.x;
-      key[e] = v.y;
-      alive |= 1u << e;
-    } else {
-      idx[e] = -1;
-      key[e] = 0xFFFFFFFFu;
-    }
-  }
-  uint32_t* hc = st.hist;
-  uint32_t* hn = st.hist2;
-  for (int q = tid; q < 2048; q += THREADS) hn[q] = 0u;
-  __syncthreads();
+  const uint32_t nr = (n + 31u) & ~31u;  // whole warps visit every slot index
+  uint64_t commit_below = 0;             // commit keys < commit_below
+  uint32_t tie_key = 0u, ties = 0u;      // then `ties` entries with key == tie_key
+  uint32_t prefix = 0u;                  // b_0 .. b_{j-1}
+  bool resolved = false;
   for (int j = 0; j < 3 && k > 0; ++j) {
-    find_boundaries_in<THREADS>(hc, st, j == 2 ? 1024 : 2048, 1, k, 0u);
-    const int b = st.res_bin[0];
-    const uint32_t below = st.res_below[0], cnt = st.res_cnt[0];
+    const int width = j == 2 ? 10 : 11;
+    const int shift = j == 0 ? 21 : (j == 1 ? 10 : 0);  // digit j occupies bits [shift, shift+width)
+    find_boundaries<G>(hist, sc, 1 << width, 1, k, 0u);
+    const int b = sc.res_bin[0];
+    const uint32_t below = sc.res_below[0], cnt = sc.res_cnt[0];
     if (b < 0) {  // inconsistent counts: cannot happen; finish_row flags it
       k = 0;
+      resolved = true;
       break;
     }
-    // b_j = min{b : H_j(b) >= k_j} (eq. 23); commit digit < b_j (eq. 24), keep
-    // digit == b_j (eq. 25).  When H_j(b_j) == k_j the boundary group closes
-    // the quota and is committed too.
-    const bool last = below + cnt == k;
-#pragma unroll
-    for (int e = 0; e < EPT; ++e) {
-      const bool al = (alive >> e) & 1u;
-      const int dg = (int)digit(key[e], j);
-      const bool com = al && (last ? dg <= b : dg < b);
-      const bool keep = al && !last && dg == b;
-      commit_warp(st, out_row, K, com, idx[e], lt);
-      if (keep && j < 2) atomicAdd(&hn[digit(key[e], j + 1)], 1u);
-      if (!keep) alive &= ~(1u << e);
-    }
-    if (last) {
+    prefix = (prefix << width) | (uint32_t)b;
+    if (below + cnt == k) {
+      // Bucket b_j closes the quota: commit every key whose leading digits
+      // are <= (b_0 .. b_j).
+      commit_below = (uint64_t)(prefix + 1u) << shift;
       k = 0;
+      resolved = true;
       break;
     }
     k -= below;
-    __syncthreads();  // next histogram complete; the finder is done with hc
-    uint32_t* t = hc;
-    hc = hn;
-    hn = t;
-    if (j < 1)
-      for (int q = tid; q < 2048; q += THREADS) hn[q] = 0u;  // ordered by the next finder's barrier
+    if (j == 2) {
+      commit_below = prefix;  // the full key T*
+      tie_key = prefix;
+      ties = k;
+      resolved = true;
+      break;
+    }
+    // h_{j+1} over Q_{j+1} = entries whose digits 0..j equal prefix.
+    G::sync();  // the finder is done with hist
+    clear_hist<G>(hist, 2048);
+    G::sync();
+    for (uint32_t p = tid; p < n; p += G::kThreads) {
+      int32_t i;
+      uint32_t d;
+      F.get(p, i, d);
+      if ((d >> shift) == prefix) atomicAdd(&hist[digit(d, j + 1)], 1u);
+    }
+    G::sync();
   }
-  if (k > 0) {
-    // After the last digit every alive key is identical: take the first k in
-    // (thread, slot) order.
-    const uint32_t c = (uint32_t)__popc(alive);
-    uint32_t incl = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t v = __shfl_up_sync(kFull, incl, o);
-      if (lane >= o) incl += v;
-    }
-    if (lane == 31) st.warp_sums[warp] = incl;
-    __syncthreads();
-    uint32_t w = lane < THREADS / 32 ? st.warp_sums[lane] : 0u;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t v = __shfl_up_sync(kFull, w, o);
-      if (lane >= o) w += v;
-    }
-    uint32_t rank = (warp ? __shfl_sync(kFull, w, warp - 1) : 0u) + incl - c;
-#pragma unroll
-    for (int e = 0; e < EPT; ++e) {
-      const bool al = (alive >> e) & 1u;
-      commit_warp(st, out_row, K, al && rank < k, idx[e], lt);
-      rank += al ? 1u : 0u;
+  if (resolved) {
+    if (tid == 0) sl.n_keep = 0u;
+    G::sync();
+    for (uint32_t p = tid; p < nr; p += G::kThreads) {
+      int32_t i = -1;
+      uint32_t d = 0xFFFFFFFFu;
+      if (p < n) F.get(p, i, d);
+      const bool in = p < n;
+      const bool com = in && (uint64_t)d < commit_below;
+      const bool tie = in && ties > 0u && d == tie_key;
+      const uint32_t tb = __ballot_sync(kFull, tie);
+      bool take = false;
+      if (tb) {
+        uint32_t base = 0u;
+        if ((threadIdx.x & 31) == 0) base = atomicAdd(&sl.n_keep, (uint32_t)__popc(tb));
+        base = __shfl_sync(kFull, base, 0);
+        take = tie && base + (uint32_t)__popc(tb & lt) < ties;
+      }
+      commit_warp(&sl.n_out, out_row, K, com || take, i, lt);
     }
   }
-  __syncthreads();
+  G::sync();
 }
 
 // ----------------------------------------------------------------------------
 // Row-level building blocks
 // ----------------------------------------------------------------------------
 
-template <int THREADS>
+template <class G>
 __device__ void write_pad_row(int32_t* out_row, int L, int K) {
-  for (int t = threadIdx.x; t < K; t += THREADS) out_row[t] = t < L ? t : -1;
+  for (int t = G::rank(); t < K; t += G::kThreads) out_row[t] = t < L ? t : -1;
 }
 
+// Route record of a row (written by one thread).
 __device__ __forceinline__ void write_trace(const Params& p, int row, int route, int tau0, int tau1,
                                             int c0, int c1, int tstar, int e0, int q0) {
-  if (p.trace == nullptr || threadIdx.x != 0) return;
+  if (p.trace == nullptr) return;
   int32_t* t = p.trace + (int64_t)row * EXACT_TOPK_TRACE_FIELDS;
   t[0] = route;
   t[1] = tau0;
@@ -836,76 +820,89 @@ __device__ __forceinline__ void write_trace(const Params& p, int row, int route,
   t[7] = q0;
 }
 
-// Final guard: every slot must be written exactly once.
-template <int THREADS>
-__device__ void finish_row(const Params& p, RowState& st, int32_t* out_row) {
-  __syncthreads();
-  const uint32_t used = st.n_out;
+__device__ __forceinline__ void write_slot_trace(const Params& p, const Slot& sl) {
+  write_trace(p, sl.row, sl.route, sl.tau0, sl.tau1, sl.c0, sl.c1, sl.tstar, sl.e0, sl.q0n);
+}
+
+// Final guard: every output slot must be written exactly once.
+template <class G>
+__device__ void finish_row(const Params& p, Slot& sl, int32_t* out_row) {
+  G::sync();
+  const uint32_t used = sl.n_out;
   if (used != (uint32_t)p.K) {
-    for (uint32_t t = used + threadIdx.x; t < (uint32_t)p.K; t += THREADS) out_row[t] = -1;
-    if (threadIdx.x == 0) flag_status(p.counters, 1);
+    for (uint32_t t = used + G::rank(); t < (uint32_t)p.K; t += G::kThreads) out_row[t] = -1;
+    if (G::rank() == 0) flag_status(p.counters, 1);
   }
-  __syncthreads();
+  G::sync();
 }
 
-// Cutoffs of the exact coarse boundary tau* (warps 0 and 1 in parallel):
-// cut[1] admits c <= tau*, cut[0] admits c < tau* (none when tau* == 0).
-template <int THREADS>
-__device__ void exact_cutoffs(RowState& st, int tstar) {
-  const int warp = threadIdx.x >> 5;
+// Cutoffs of the exact coarse boundary tau* (group warps 0 and 1):
+// T1 admits c <= tau*, T0 admits c < tau* (none when tau* == 0).
+template <class G>
+__device__ void exact_cutoffs(Slot& sl, int tstar) {
+  const int warp = G::rank() >> 5;
   if (warp == 0) {
-    const uint32_t t = cutoff_for_bin_warp(tstar);
-    if ((threadIdx.x & 31) == 0) st.cut[1] = t;
+    const uint32_t t = cutoff_fast_warp(tstar);
+    if ((G::rank() & 31) == 0) sl.T1 = t;
   } else if (warp == 1) {
-    const uint32_t t = tstar > 0 ? cutoff_for_bin_warp(tstar - 1) : 0u;
-    if ((threadIdx.x & 31) == 0) st.cut[0] = t;
+    const uint32_t t = tstar > 0 ? cutoff_fast_warp(tstar - 1) : 0u;
+    if ((G::rank() & 31) == 0) sl.T0 = t;
   }
-  __syncthreads();
+  G::sync();
 }
 
-// Exact coarse recovery over row[0, L) followed by refinement (eq. 20).
-// Leaves st.n_out == K.  Returns tau*, |E0| and |Q0| through the out params.
-template <int THREADS>
-__device__ void exact_route(const Params& p, const float* row, int L, const Frontier& F, RowState& st,
-                            int32_t* out_row, int& tstar, int& e0, int& q0n) {
+// Exact coarse recovery over row[0, L) (eq. 20): coarse histogram, tau* =
+// min{b : C(b) >= K}, then one pass that commits c < tau* to the output (E0)
+// and keeps c == tau* as the frontier Q0 with its digit-0 histogram h0.
+// Leaves the refinement interface in the slot: n_front = |Q0|, n_out = |E0|.
+template <class G>
+__device__ void exact_recovery(const Params& p, const float* row, int L, const Frontier& F,
+                               uint32_t* hist, GroupScratch& sc, Slot& sl, int32_t* out_row,
+                               uint32_t* queues) {
   const int K = p.K;
-  clear_hist<THREADS>(st, 2048);
-  if (threadIdx.x == 0) {
-    st.n_front = 0u;
-    st.n_out = 0u;
+  clear_hist<G>(hist, 2048);
+  if (G::rank() == 0) {
+    sl.n_front = 0u;
+    sl.n_out = 0u;
   }
-  __syncthreads();
-  scan_coarse_hist<THREADS>(row, 0, L, st);
-  __syncthreads();
-  find_boundaries<THREADS>(st, 2048, 1, (uint32_t)K, 0u);
-  tstar = st.res_bin[0];
-  e0 = (int)st.res_below[0];
-  exact_cutoffs<THREADS>(st, tstar);
-  const uint32_t tlo = st.cut[0], thi = st.cut[1];
-  clear_hist<THREADS>(st, 2048);
-  __syncthreads();
+  G::sync();
+  scan_coarse_hist<G>(row, 0, L, hist);
+  G::sync();
+  find_boundaries<G>(hist, sc, 2048, 1, (uint32_t)K, 0u);
+  const int tstar = sc.res_bin[0];
+  const int e0 = (int)sc.res_below[0];
+  exact_cutoffs<G>(sl, tstar);
+  const uint32_t tlo = sl.T0, thi = sl.T1;
+  clear_hist<G>(hist, 2048);
+  G::sync();
   CommitSink commit_sink{out_row, (uint32_t)K};
-  FrontierSink front_sink{F, st.hist};
-  scan_two_class<THREADS>(row, 0, L, tlo, thi, tstar > 0, &st.n_out, &st.n_front, queue_area(p), commit_sink,
-                          front_sink);
-  __syncthreads();
-  q0n = (int)st.n_front;
-  refine<THREADS>(F, st.n_front, (uint32_t)(K - e0), st, out_row, K);
+  FrontierSink front_sink{F, hist};
+  scan_two_class<G>(row, 0, L, tlo, thi, tstar > 0, &sl.n_out, &sl.n_front, queues, commit_sink,
+                    front_sink);
+  G::sync();
+  if (G::rank() == 0) {
+    sl.tstar = tstar;
+    sl.e0 = e0;
+    sl.q0n = (int)sl.n_front;
+  }
+  G::sync();
 }
 
-// Row-local exact route with the row resident in registers (section 5.5,
+// Exact coarse recovery with the row resident in registers (section 5.5,
 // "Row-local exact": the short-row specialization keeps aligned score vectors
 // in registers across boundary construction and classification).
-template <int THREADS, int VPT>
-__device__ void exact_route_resident(const Params& p, const float* row, int L, const Frontier& F,
-                                     RowState& st, int32_t* out_row, int& tstar, int& e0, int& q0n) {
+template <class G, int VPT>
+__device__ void exact_recovery_resident(const Params& p, const float* row, int L,
+                                        const Frontier& F, uint32_t* hist, GroupScratch& sc,
+                                        Slot& sl, int32_t* out_row) {
   const int K = p.K;
-  const int tid = threadIdx.x;
+  const int tid = G::rank();
+  const uint32_t lt = lanemask_lt();
   uint32_t v[VPT];
   const bool aligned = (reinterpret_cast<uintptr_t>(row) & 31u) == 0u;
 #pragma unroll
   for (int g = 0; g < VPT / 8; ++g) {
-    const int i0 = (g * THREADS + tid) * 8;
+    const int i0 = (g * G::kThreads + tid) * 8;
     if (aligned && i0 + 7 < L) {
       ld_stream8(row + i0, v + 8 * g);
     } else {
@@ -913,51 +910,52 @@ __device__ void exact_route_resident(const Params& p, const float* row, int L, c
       for (int e = 0; e < 8; ++e) v[g * 8 + e] = (i0 + e < L) ? ld_stream1(row + i0 + e) : 0u;
     }
   }
-  clear_hist<THREADS>(st, 2048);
+  clear_hist<G>(hist, 2048);
   if (tid == 0) {
-    st.n_front = 0u;
-    st.n_out = 0u;
+    sl.n_front = 0u;
+    sl.n_out = 0u;
   }
-  __syncthreads();
+  G::sync();
 #pragma unroll
   for (int g = 0; g < VPT / 8; ++g) {
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      const int i = (g * THREADS + tid) * 8 + e;
-      if (i < L) atomicAdd(&st.hist[coarse_bin(v[g * 8 + e])], 1u);
+      const int i = (g * G::kThreads + tid) * 8 + e;
+      if (i < L) atomicAdd(&hist[coarse_bin(v[g * 8 + e])], 1u);
     }
   }
-  __syncthreads();
-  find_boundaries<THREADS>(st, 2048, 1, (uint32_t)K, 0u);
-  tstar = st.res_bin[0];
-  e0 = (int)st.res_below[0];
-  exact_cutoffs<THREADS>(st, tstar);
-  clear_hist<THREADS>(st, 2048);
-  __syncthreads();
-  const uint32_t tlo = st.cut[0], thi = st.cut[1];
+  G::sync();
+  find_boundaries<G>(hist, sc, 2048, 1, (uint32_t)K, 0u);
+  const int tstar = sc.res_bin[0];
+  const int e0 = (int)sc.res_below[0];
+  exact_cutoffs<G>(sl, tstar);
+  clear_hist<G>(hist, 2048);
+  G::sync();
+  const uint32_t tlo = sl.T0, thi = sl.T1;
   const bool has_lo = tstar > 0;
 #pragma unroll
   for (int g = 0; g < VPT / 8; ++g) {
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      const int i = (g * THREADS + tid) * 8 + e;
-      if (i < L) {
-        const uint32_t d = desc_key(v[g * 8 + e]);
-        if (d <= thi) {
-          if (has_lo && d <= tlo) {
-            commit(st, out_row, K, i);
-          } else {
-            const uint32_t q = atomicAdd(&st.n_front, 1u);
-            F.put(q, i, d);
-            atomicAdd(&st.hist[d >> 21], 1u);
-          }
-        }
+      const int i = (g * G::kThreads + tid) * 8 + e;
+      const uint32_t d = desc_key(v[g * 8 + e]);
+      const bool valid = i < L && d <= thi;
+      const bool com = valid && has_lo && d <= tlo;
+      commit_warp(&sl.n_out, out_row, K, com, i, lt);
+      if (valid && !com) {
+        const uint32_t q = atomicAdd(&sl.n_front, 1u);
+        F.put(q, i, d);
+        atomicAdd(&hist[d >> 21], 1u);
       }
     }
   }
-  __syncthreads();
-  q0n = (int)st.n_front;
-  refine<THREADS>(F, st.n_front, (uint32_t)(K - e0), st, out_row, K);
+  G::sync();
+  if (tid == 0) {
+    sl.tstar = tstar;
+    sl.e0 = e0;
+    sl.q0n = (int)sl.n_front;
+  }
+  G::sync();
 }
 
 __device__ __forceinline__ int view_phase(int row, int s, int s_bits) {
@@ -969,50 +967,66 @@ __device__ __forceinline__ int view_size(int L, int a, int s) {
   return L > a ? (L - a + s - 1) / s : 0;
 }
 
-// Phase 1 (section 4.2, eqs. 13-15): coarse histogram of the view
-// V = {i < L : i = a_r (mod s)} and the boundaries tau0 / tau1 with their
-// inclusive cutoffs.  Each thread issues up to 8 view loads before using any.
-// Entered with a cleared histogram; leaves it dirty.
-template <int THREADS>
-__device__ void sample_view(const Params& p, const float* row, int L, int a, RowState& st) {
+// Phase 1 (section 4.2, eqs. 13-15) by group G: coarse histogram of the view
+// V = {i < L : i = a_r (mod s)}, the boundaries tau0 / tau1 and their
+// inclusive cutoffs, written to the slot.  Each thread issues up to 8 view
+// loads before using any.  Entered with a cleared histogram; leaves it dirty.
+template <class G>
+__device__ void sample_view(const Params& p, const float* row, int L, int a, uint32_t* hist,
+                            GroupScratch& sc, Slot& sl, const uint32_t* pre = nullptr,
+                            int npre = 0) {
   const int nv = view_size(L, a, p.s);
-  const int tid = threadIdx.x;
-  for (int t0 = 0; t0 < nv; t0 += 8 * THREADS) {
+  const int tid = G::rank();
+  // Entries [0, npre) were copied to `pre` by this same thread layout
+  // (entry t by rank t mod kThreads), so each thread reads only its own.
+  if (npre > 0) {
+    cp_async_wait_all();
+    for (int t = tid; t < npre; t += G::kThreads) atomicAdd(&hist[coarse_bin(pre[t])], 1u);
+  }
+  for (int t0 = npre; t0 < nv; t0 += 8 * G::kThreads) {
     uint32_t u[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const int t = t0 + k * THREADS + tid;
+      const int t = t0 + k * G::kThreads + tid;
       u[k] = t < nv ? __ldg(reinterpret_cast<const unsigned int*>(row) + a + (int64_t)t * p.s) : 0u;
     }
 #pragma unroll
     for (int k = 0; k < 8; ++k)
-      if (t0 + k * THREADS + tid < nv) atomicAdd(&st.hist[coarse_bin(u[k])], 1u);
+      if (t0 + k * G::kThreads + tid < nv) atomicAdd(&hist[coarse_bin(u[k])], 1u);
   }
-  __syncthreads();
-  find_boundaries<THREADS>(st, 2048, 2, (uint32_t)p.q0, (uint32_t)p.q1);
+  G::sync();
+  find_boundaries<G>(hist, sc, 2048, 2, (uint32_t)p.q0, (uint32_t)p.q1);
   const int warp = tid >> 5;
   if (warp == 0) {
-    const uint32_t t = cutoff_for_bin_warp(st.res_bin[0]);
-    if ((tid & 31) == 0) st.cut[0] = t;
-  } else if (warp == 1 && p.dual) {
-    const uint32_t t = cutoff_for_bin_warp(st.res_bin[1]);
-    if ((tid & 31) == 0) st.cut[1] = t;
+    const uint32_t t = cutoff_fast_warp(sc.res_bin[0]);
+    if ((tid & 31) == 0) {
+      sl.T0 = t;
+      sl.tau0 = sc.res_bin[0];
+    }
+  } else if (warp == 1) {
+    const uint32_t t = p.dual ? cutoff_fast_warp(sc.res_bin[1]) : 0u;
+    if ((tid & 31) == 0) {
+      sl.T1 = t;
+      sl.tau1 = p.dual ? sc.res_bin[1] : -1;
+    }
   }
-  __syncthreads();
+  G::sync();
 }
 
 // Optional guess source (previous-step Top-K): the worst coarse bin of the K
 // guessed scores, valid only when all K entries are positions of this row.
-template <int THREADS>
-__device__ bool guess_bin(const Params& p, const float* row, int L, int r, RowState& st) {
-  if (threadIdx.x == 0) {
-    st.gmax = -1;
-    st.ginvalid = 0;
+// On success the slot holds tau0 = that bin and T0 = its cutoff.
+template <class G>
+__device__ bool guess_bin(const Params& p, const float* row, int L, int r, GroupScratch& sc,
+                          Slot& sl) {
+  if (G::rank() == 0) {
+    sc.gmax = -1;
+    sc.ginvalid = 0;
   }
-  __syncthreads();
+  G::sync();
   const int32_t* g = p.prev + (int64_t)r * p.K;
   int worst = -1, invalid = 0;
-  for (int t = threadIdx.x; t < p.K; t += THREADS) {
+  for (int t = G::rank(); t < p.K; t += G::kThreads) {
     const int32_t idx = g[t];
     if (idx < 0 || idx >= L) {
       invalid = 1;
@@ -1021,101 +1035,48 @@ __device__ bool guess_bin(const Params& p, const float* row, int L, int r, RowSt
       worst = max(worst, coarse_bin(u));
     }
   }
-  if (invalid) atomicOr(&st.ginvalid, 1);
-  if (worst >= 0) atomicMax(&st.gmax, worst);
-  __syncthreads();
-  const bool ok = st.ginvalid == 0;
-  if (ok && threadIdx.x < 32) {
-    const uint32_t t = cutoff_for_bin_warp(st.gmax);
-    if (threadIdx.x == 0) st.cut[0] = t;
+  if (invalid) atomicOr(&sc.ginvalid, 1);
+  if (worst >= 0) atomicMax(&sc.gmax, worst);
+  G::sync();
+  const bool ok = sc.ginvalid == 0;
+  if (ok && G::rank() < 32) {
+    const uint32_t t = cutoff_fast_warp(sc.gmax);
+    if (G::rank() == 0) {
+      sl.T0 = t;
+      sl.tau0 = sc.gmax;
+    }
   }
-  __syncthreads();
+  G::sync();
   return ok;
 }
 
-// One row on the persistent sampled body: Phases 1-3 with band rescue and
-// exact recovery, all under one CTA (section 5.5, "Persistent sampled").
-template <int THREADS>
-__device__ void sampled_row(const Params& p, int r, const Frontier& F, RowState& st) {
-  const int K = p.K;
-  const float* row = p.logits + (int64_t)r * p.pitch;
-  int L = p.ke[r];
-  L = L < 0 ? 0 : (L > p.N ? p.N : L);
-  int32_t* out_row = p.out + (int64_t)r * K;
-  if (L <= K) {
-    write_pad_row<THREADS>(out_row, L, K);
-    write_trace(p, r, EXACT_TOPK_ROUTE_PAD, -1, -1, -1, -1, -1, -1, -1);
-    return;
-  }
-  clear_hist<THREADS>(st, 2048);
-  if (threadIdx.x == 0) {
-    st.n_front = 0u;
-    st.n_out = 0u;
-    st.n_drop = 0u;
-  }
-  __syncthreads();
+__device__ __forceinline__ int live_rows(const Params& p) {
+  int m = p.num_valid_rows ? *p.num_valid_rows : p.M_cap;
+  return m < 0 ? 0 : (m > p.M_cap ? p.M_cap : m);
+}
 
-  FrontierSink front_sink{F, st.hist};
-  DropSink drop;
-  int route = -1, tau0 = -1, tau1 = -1, c0 = -1, c1 = -1;
-  bool certified = false;
-  if (p.prev != nullptr && guess_bin<THREADS>(p, row, L, r, st)) {
-    tau0 = st.gmax;
-    const uint32_t T = st.cut[0];
-    scan_two_class<THREADS>(row, 0, L, T, T, false, &st.n_drop, &st.n_front, queue_area(p), drop,
-                            front_sink);
-    __syncthreads();
-    c0 = (int)st.n_front;
-    certified = c0 >= K;
-    route = certified ? EXACT_TOPK_ROUTE_GUESS : EXACT_TOPK_ROUTE_GUESS_EXACT;
+__device__ __forceinline__ int row_length(const Params& p, int r) {
+  const int L = p.ke[r];
+  return L < 0 ? 0 : (L > p.N ? p.N : L);
+}
+
+__device__ __forceinline__ Frontier make_frontier(const Params& p, uint2* smem_part,
+                                                  int64_t slice) {
+  Frontier F;
+  F.s = smem_part;
+  F.cap = (uint32_t)p.cap;
+  if (p.ws != nullptr) {
+    F.g = p.ws + slice * p.N;
+    F.gcap = (uint32_t)p.N;
   } else {
-    const int a = view_phase(r, p.s, p.s_bits);
-    const int nv = view_size(L, a, p.s);
-    const int qmax = p.dual ? p.q1 : p.q0;
-    if (nv >= qmax) {
-      sample_view<THREADS>(p, row, L, a, st);
-      tau0 = st.res_bin[0];
-      tau1 = p.dual ? st.res_bin[1] : -1;
-      const uint32_t T0 = st.cut[0], T1 = st.cut[1];
-      clear_hist<THREADS>(st, 2048);
-      __syncthreads();
-      // Phase 2: admit d <= T0, persist candidates, build h0 (eqs. 16-17).
-      scan_two_class<THREADS>(row, 0, L, T0, T0, false, &st.n_drop, &st.n_front, queue_area(p),
-                              drop, front_sink);
-      __syncthreads();
-      c0 = (int)st.n_front;
-      if (c0 >= K) {
-        route = EXACT_TOPK_ROUTE_PRIMARY;
-        certified = true;
-      } else if (p.dual) {
-        // Band rescue (eqs. 18-19): a second pass appends only T0 < d <= T1.
-        if (T1 > T0)
-          scan_two_class<THREADS>(row, 0, L, T0, T1, true, &st.n_drop, &st.n_front, queue_area(p), drop,
-                                  front_sink);
-        __syncthreads();
-        c1 = (int)st.n_front;
-        certified = c1 >= K;
-        route = certified ? EXACT_TOPK_ROUTE_BAND : EXACT_TOPK_ROUTE_EXACT_AFTER_BAND;
-      } else {
-        route = EXACT_TOPK_ROUTE_EXACT_NO_BAND;
-      }
-    } else {
-      route = EXACT_TOPK_ROUTE_DIRECT_EXACT;
-    }
+    F.g = nullptr;
+    F.gcap = 0u;
   }
-  int tstar = -1, e0 = 0, q0n;
-  if (certified) {
-    q0n = (int)st.n_front;  // eq. 21: E0 = {}, Q0 = A(tau), k0 = K, h0 = h0^(tau)
-    refine<THREADS>(F, st.n_front, (uint32_t)K, st, out_row, K);
-  } else {
-    exact_route<THREADS>(p, row, L, F, st, out_row, tstar, e0, q0n);
-  }
-  finish_row<THREADS>(p, st, out_row);
-  write_trace(p, r, route, tau0, tau1, c0, c1, tstar, e0, q0n);
+  return F;
 }
 
 // Last CTA out resets the queue head and the exit counter (section 5.5:
-// "persistent counters are restored on device").
+// "persistent counters are restored on device").  Entered by the whole CTA.
 __device__ void exit_protocol(int32_t* counters) {
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -1128,47 +1089,153 @@ __device__ void exit_protocol(int32_t* counters) {
   }
 }
 
-__device__ __forceinline__ int live_rows(const Params& p) {
-  int m = p.num_valid_rows ? *p.num_valid_rows : p.M_cap;
-  return m < 0 ? 0 : (m > p.M_cap ? p.M_cap : m);
-}
-
-__device__ __forceinline__ RowState& row_state() {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  return *reinterpret_cast<RowState*>(smem_raw);
-}
-
-__device__ __forceinline__ Frontier make_frontier(const Params& p, int64_t slice) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  Frontier F;
-  F.s = reinterpret_cast<uint2*>(smem_raw + sizeof(RowState));
-  F.cap = (uint32_t)p.cap;
-  if (p.ws != nullptr) {
-    F.g = p.ws + slice * p.N;
-    F.gcap = (uint32_t)p.N;
-  } else {
-    F.g = nullptr;
-    F.gcap = 0u;
-  }
-  return F;
-}
-
 // ----------------------------------------------------------------------------
 // Kernel 1: persistent sampled
 // ----------------------------------------------------------------------------
 
-__global__ void __launch_bounds__(kPersistentThreads, ETK_SAMPLED_MIN_CTAS) persistent_sampled_kernel(Params p) {
-  RowState& st = row_state();
-  const Frontier F = make_frontier(p, blockIdx.x);
+// One CTA owns a row for all three phases (section 5.5, "Persistent sampled"):
+// Phase 1, the complete-row pass with its certification (band rescue, exact
+// coarse recovery), and Phase 3.  Rows after the first wave are claimed from a
+// device counter in completion order.
+// Claims the next row and starts copying its view (Phase 1 input) into
+// shared memory, so that the copies overlap this row's refinement.
+__device__ int claim_and_prefetch(const Params& p, int M, Slot& sl, GroupScratch& sc,
+                                  uint32_t* view) {
+  if (threadIdx.x == 0) sc.bcast = (int)gridDim.x + atomicAdd(p.counters + kCtrQueue, 1);
+  __syncthreads();
+  const int nr = sc.bcast;
+  int npre = 0;
+  if (nr < M && p.prev == nullptr) {
+    const int L = row_length(p, nr);
+    const int a = view_phase(nr, p.s, p.s_bits);
+    const int nv = view_size(L, a, p.s);
+    const int qmax = p.dual ? p.q1 : p.q0;
+    if (L > p.K && nv >= qmax) {
+      npre = nv < kViewPrefetch ? nv : kViewPrefetch;
+      npre -= npre % kPersistentThreads;  // whole rounds of the thread layout
+      const float* row = p.logits + (int64_t)nr * p.pitch;
+      for (int t = threadIdx.x; t < npre; t += kPersistentThreads)
+        cp_async4(view + t, row + a + (int64_t)t * p.s);
+      cp_async_commit();
+    }
+  }
+  __syncthreads();  // everyone has read bcast
+  if (threadIdx.x == 0) {
+    sl.pf_row = npre > 0 ? nr : -1;
+    sl.pf_n = npre;
+  }
+  return nr;
+}
+
+__device__ void simple_row(const Params& p, int r, Slot& sl, const Frontier& F, uint32_t* hist,
+                           GroupScratch& sc, uint32_t* queues, uint32_t* view, int M,
+                           int& next) {
+  using G = CtaGroup<kPersistentThreads>;
+  const int K = p.K;
+  const float* row = p.logits + (int64_t)r * p.pitch;
+  const int L = row_length(p, r);
+  int32_t* out_row = p.out + (int64_t)r * K;
+  const bool have_pf = sl.pf_row == r;
+  const int npre = have_pf ? sl.pf_n : 0;
+  if (L <= K) {
+    write_pad_row<G>(out_row, L, K);
+    if (threadIdx.x == 0) write_trace(p, r, EXACT_TOPK_ROUTE_PAD, -1, -1, -1, -1, -1, -1, -1);
+    next = claim_and_prefetch(p, M, sl, sc, view);
+    return;
+  }
+  G::sync();  // every thread has read the prefetch record
+  clear_hist<G>(hist, 2048);
+  if (threadIdx.x == 0) {
+    sl.row = r;
+    sl.L = L;
+    sl.n_front = 0u;
+    sl.n_out = 0u;
+    sl.n_drop = 0u;
+    sl.tau0 = -1;
+    sl.tau1 = -1;
+    sl.c0 = -1;
+    sl.c1 = -1;
+    sl.tstar = -1;
+    sl.e0 = 0;
+  }
+  G::sync();
+  FrontierSink front_sink{F, hist};
+  DropSink drop;
+  bool exact = false;
+  int route;
+  if (p.prev != nullptr && guess_bin<G>(p, row, L, r, sc, sl)) {
+    const uint32_t T = sl.T0;
+    scan_two_class<G>(row, 0, L, T, T, false, &sl.n_drop, &sl.n_front, queues, drop, front_sink);
+    G::sync();
+    const uint32_t c0 = sl.n_front;
+    route = c0 >= (uint32_t)K ? EXACT_TOPK_ROUTE_GUESS : EXACT_TOPK_ROUTE_GUESS_EXACT;
+    if (threadIdx.x == 0) sl.c0 = (int)c0;
+  } else {
+    const int a = view_phase(r, p.s, p.s_bits);
+    const int qmax = p.dual ? p.q1 : p.q0;
+    if (view_size(L, a, p.s) >= qmax) {
+      sample_view<G>(p, row, L, a, hist, sc, sl, view, npre);
+      const uint32_t T0 = sl.T0, T1 = sl.T1;
+      clear_hist<G>(hist, 2048);
+      G::sync();
+      // Phase 2: admit d <= T0, persist candidates, build h0 (eqs. 16-17).
+      scan_two_class<G>(row, 0, L, T0, T0, false, &sl.n_drop, &sl.n_front, queues, drop,
+                        front_sink);
+      G::sync();
+      const uint32_t c0 = sl.n_front;
+      if (c0 >= (uint32_t)K) {
+        route = EXACT_TOPK_ROUTE_PRIMARY;
+      } else if (p.dual) {
+        // Band rescue (eqs. 18-19): a second pass appends only T0 < d <= T1.
+        if (T1 > T0)
+          scan_two_class<G>(row, 0, L, T0, T1, true, &sl.n_drop, &sl.n_front, queues, drop,
+                            front_sink);
+        G::sync();
+        const uint32_t c1 = sl.n_front;
+        route = c1 >= (uint32_t)K ? EXACT_TOPK_ROUTE_BAND : EXACT_TOPK_ROUTE_EXACT_AFTER_BAND;
+        if (threadIdx.x == 0) sl.c1 = (int)c1;
+      } else {
+        route = EXACT_TOPK_ROUTE_EXACT_NO_BAND;
+      }
+      if (threadIdx.x == 0) sl.c0 = (int)c0;
+    } else {
+      route = EXACT_TOPK_ROUTE_DIRECT_EXACT;
+    }
+  }
+  exact = route == EXACT_TOPK_ROUTE_EXACT_AFTER_BAND || route == EXACT_TOPK_ROUTE_EXACT_NO_BAND ||
+          route == EXACT_TOPK_ROUTE_GUESS_EXACT || route == EXACT_TOPK_ROUTE_DIRECT_EXACT;
+  if (threadIdx.x == 0) {
+    sl.route = route;
+    sl.q0n = (int)sl.n_front;  // eq. 21: E0 = {}, Q0 = A(tau), k0 = K
+  }
+  G::sync();
+  if (exact) exact_recovery<G>(p, row, L, F, hist, sc, sl, out_row, queues);
+  next = claim_and_prefetch(p, M, sl, sc, view);
+  refine<G>(F, sl.n_front, (uint32_t)(K - sl.e0), hist, sc, sl, out_row, K);
+  finish_row<G>(p, sl, out_row);
+  if (threadIdx.x == 0) write_slot_trace(p, sl);
+}
+
+__global__ void __launch_bounds__(kPersistentThreads, 2) persistent_sampled_kernel(Params p) {
+  unsigned char* sm = smem_base();
+  const SmemLayout lay = smem_layout(EXACT_TOPK_FAMILY_PERSISTENT_SAMPLED, p.cap);
+  Slot& sl = *reinterpret_cast<Slot*>(sm + lay.slots);
+  GroupScratch& sc = *reinterpret_cast<GroupScratch*>(sm + lay.scratch);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(sm + lay.hist);
+  uint32_t* queues = reinterpret_cast<uint32_t*>(sm + lay.queues);
+  uint32_t* view = reinterpret_cast<uint32_t*>(sm + lay.view);
+  const Frontier F = make_frontier(p, reinterpret_cast<uint2*>(sm + lay.frontier), blockIdx.x);
   const int M = live_rows(p);
+  if (threadIdx.x == 0) sl.pf_row = -1;
+  __syncthreads();
   int r = blockIdx.x;
   while (r < M) {
-    sampled_row<kPersistentThreads>(p, r, F, st);
+    int next = M;
+    simple_row(p, r, sl, F, hist, sc, queues, view, M, next);
     __syncthreads();
-    if (threadIdx.x == 0) st.next_row = (int)gridDim.x + atomicAdd(p.counters + kCtrQueue, 1);
-    __syncthreads();
-    r = st.next_row;
+    r = next;
   }
+  cp_async_wait_all();  // no copy may be left in flight at exit
   exit_protocol(p.counters);
 }
 
@@ -1177,33 +1244,40 @@ __global__ void __launch_bounds__(kPersistentThreads, ETK_SAMPLED_MIN_CTAS) pers
 // ----------------------------------------------------------------------------
 
 __global__ void __launch_bounds__(kRowLocalThreads, 1) row_local_exact_kernel(Params p) {
-  RowState& st = row_state();
-  const Frontier F = make_frontier(p, blockIdx.x);
+  using G = CtaGroup<kRowLocalThreads>;
+  unsigned char* sm = smem_base();
+  const SmemLayout lay = smem_layout(EXACT_TOPK_FAMILY_ROW_LOCAL_EXACT, p.cap);
+  Slot& sl = *reinterpret_cast<Slot*>(sm + lay.slots);
+  GroupScratch& sc = *reinterpret_cast<GroupScratch*>(sm + lay.scratch);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(sm + lay.hist);
+  uint32_t* queues = reinterpret_cast<uint32_t*>(sm + lay.queues);
+  const Frontier F = make_frontier(p, reinterpret_cast<uint2*>(sm + lay.frontier), blockIdx.x);
   const int M = live_rows(p);
   int r = blockIdx.x;
   while (r < M) {
     const int K = p.K;
     const float* row = p.logits + (int64_t)r * p.pitch;
-    int L = p.ke[r];
-    L = L < 0 ? 0 : (L > p.N ? p.N : L);
+    const int L = row_length(p, r);
     int32_t* out_row = p.out + (int64_t)r * K;
     if (L <= K) {
-      write_pad_row<kRowLocalThreads>(out_row, L, K);
-      write_trace(p, r, EXACT_TOPK_ROUTE_PAD, -1, -1, -1, -1, -1, -1, -1);
+      write_pad_row<G>(out_row, L, K);
+      if (threadIdx.x == 0) write_trace(p, r, EXACT_TOPK_ROUTE_PAD, -1, -1, -1, -1, -1, -1, -1);
     } else {
-      int tstar, e0, q0n;
       if (L <= kRowLocalResident)
-        exact_route_resident<kRowLocalThreads, kRowLocalResident / kRowLocalThreads>(
-            p, row, L, F, st, out_row, tstar, e0, q0n);
+        exact_recovery_resident<G, kRowLocalResident / kRowLocalThreads>(p, row, L, F, hist, sc,
+                                                                          sl, out_row);
       else
-        exact_route<kRowLocalThreads>(p, row, L, F, st, out_row, tstar, e0, q0n);
-      finish_row<kRowLocalThreads>(p, st, out_row);
-      write_trace(p, r, EXACT_TOPK_ROUTE_DIRECT_EXACT, -1, -1, -1, -1, tstar, e0, q0n);
+        exact_recovery<G>(p, row, L, F, hist, sc, sl, out_row, queues);
+      refine<G>(F, sl.n_front, (uint32_t)(K - sl.e0), hist, sc, sl, out_row, K);
+      finish_row<G>(p, sl, out_row);
+      if (threadIdx.x == 0)
+        write_trace(p, r, EXACT_TOPK_ROUTE_DIRECT_EXACT, -1, -1, -1, -1, sl.tstar, sl.e0, sl.q0n);
     }
     __syncthreads();
-    if (threadIdx.x == 0) st.next_row = (int)gridDim.x + atomicAdd(p.counters + kCtrQueue, 1);
+    if (threadIdx.x == 0) sc.bcast = (int)gridDim.x + atomicAdd(p.counters + kCtrQueue, 1);
     __syncthreads();
-    r = st.next_row;
+    r = sc.bcast;
+    __syncthreads();
   }
   exit_protocol(p.counters);
 }
@@ -1240,8 +1314,17 @@ struct SegmentBackSink {
   }
 };
 
-__global__ void __launch_bounds__(kKvSplitThreads, ETK_SAMPLED_MIN_CTAS) kv_split_kernel(Params p) {
-  RowState& st = row_state();
+__global__ void __launch_bounds__(kKvSplitThreads, 2) kv_split_kernel(Params p) {
+  using G = CtaGroup<kKvSplitThreads>;
+  unsigned char* sm = smem_base();
+  const SmemLayout lay = smem_layout(EXACT_TOPK_FAMILY_KV_SPLIT, p.cap);
+  Slot& sl = *reinterpret_cast<Slot*>(sm + lay.slots);
+  GroupScratch& sc = *reinterpret_cast<GroupScratch*>(sm + lay.scratch);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(sm + lay.hist);
+  uint32_t* run_pre = reinterpret_cast<uint32_t*>(sm + lay.runs);
+  uint32_t* run_c0 = run_pre + kMaxSplits + 1;
+  uint32_t* run_cb = run_c0 + kMaxSplits;
+  uint32_t* queues = reinterpret_cast<uint32_t*>(sm + lay.queues);
   const int r = blockIdx.y;
   const int seg = blockIdx.x;
   const int P = p.P;
@@ -1249,59 +1332,60 @@ __global__ void __launch_bounds__(kKvSplitThreads, ETK_SAMPLED_MIN_CTAS) kv_spli
   const int tid = threadIdx.x;
   if (r >= live_rows(p)) return;
   const float* row = p.logits + (int64_t)r * p.pitch;
-  int L = p.ke[r];
-  L = L < 0 ? 0 : (L > p.N ? p.N : L);
+  const int L = row_length(p, r);
   int32_t* out_row = p.out + (int64_t)r * K;
   // Row buffer: segment-owned candidate ranges, later the finisher's spill.
   uint2* rb = p.ws + (int64_t)r * p.N;
-  const Frontier F = make_frontier(p, r);
+  const Frontier F = make_frontier(p, reinterpret_cast<uint2*>(sm + lay.frontier), r);
 
   if (L <= K) {
     if (seg == 0) {
-      write_pad_row<kKvSplitThreads>(out_row, L, K);
-      write_trace(p, r, EXACT_TOPK_ROUTE_PAD, -1, -1, -1, -1, -1, -1, -1);
+      write_pad_row<G>(out_row, L, K);
+      if (tid == 0) write_trace(p, r, EXACT_TOPK_ROUTE_PAD, -1, -1, -1, -1, -1, -1, -1);
     }
     return;
   }
-  clear_hist<kKvSplitThreads>(st, 2048);
+  clear_hist<G>(hist, 2048);
   if (tid == 0) {
-    st.seg_c0 = 0u;
-    st.seg_cb = 0u;
-    st.n_front = 0u;
-    st.n_out = 0u;
+    sl.seg_c0 = 0u;
+    sl.seg_cb = 0u;
+    sl.n_front = 0u;
+    sl.n_out = 0u;
+    sl.tau0 = -1;
+    sl.tau1 = -1;
+    sl.e0 = 0;
+    sl.tstar = -1;
   }
-  __syncthreads();
+  G::sync();
 
   // Every segment reconstructs the same row-local proposal from r alone.
   bool guess = false;
-  int tau0 = -1, tau1 = -1;
   uint32_t T0 = 0u, T1 = 0u;
   bool use_band = false;
-  if (p.prev != nullptr && guess_bin<kKvSplitThreads>(p, row, L, r, st)) {
+  if (p.prev != nullptr && guess_bin<G>(p, row, L, r, sc, sl)) {
     guess = true;
-    tau0 = st.gmax;
-    T0 = st.cut[0];
+    T0 = sl.T0;
   } else {
     const int a = view_phase(r, p.s, p.s_bits);
-    const int nv = view_size(L, a, p.s);
     const int qmax = p.dual ? p.q1 : p.q0;
-    if (nv < qmax) {
+    if (view_size(L, a, p.s) < qmax) {
       // View unusable: the row takes the direct-exact route on one CTA.
       if (seg == 0) {
-        int tstar, e0, q0n;
-        exact_route<kKvSplitThreads>(p, row, L, F, st, out_row, tstar, e0, q0n);
-        finish_row<kKvSplitThreads>(p, st, out_row);
-        write_trace(p, r, EXACT_TOPK_ROUTE_DIRECT_EXACT, -1, -1, -1, -1, tstar, e0, q0n);
+        exact_recovery<G>(p, row, L, F, hist, sc, sl, out_row, queues);
+        refine<G>(F, sl.n_front, (uint32_t)(K - sl.e0), hist, sc, sl, out_row, K);
+        finish_row<G>(p, sl, out_row);
+        if (tid == 0)
+          write_trace(p, r, EXACT_TOPK_ROUTE_DIRECT_EXACT, -1, -1, -1, -1, sl.tstar, sl.e0,
+                      sl.q0n);
       }
       return;
     }
-    sample_view<kKvSplitThreads>(p, row, L, a, st);
-    tau0 = st.res_bin[0];
-    tau1 = p.dual ? st.res_bin[1] : -1;
-    T0 = st.cut[0];
-    T1 = st.cut[1];
+    sample_view<G>(p, row, L, a, hist, sc, sl);
+    T0 = sl.T0;
+    T1 = sl.T1;
     use_band = p.dual && T1 > T0;
   }
+  const int tau0 = sl.tau0, tau1 = guess ? -1 : sl.tau1;
 
   // Phase 2 over this segment, with the band (T0 < d <= T1) collected in the
   // same traversal: an underfilled primary needs no second pass.
@@ -1310,47 +1394,47 @@ __global__ void __launch_bounds__(kKvSplitThreads, ETK_SAMPLED_MIN_CTAS) kv_spli
   {
     SegmentFrontSink primary{rb, lo};
     SegmentBackSink band{rb, hi};
-    scan_two_class<kKvSplitThreads>(row, lo, hi, T0, use_band ? T1 : T0, true, &st.seg_c0,
-                                    &st.seg_cb, queue_area(p), primary, band);
+    scan_two_class<G>(row, lo, hi, T0, use_band ? T1 : T0, true, &sl.seg_c0, &sl.seg_cb, queues,
+                      primary, band);
   }
   __threadfence();  // every writer publishes its candidates before the arrival
-  __syncthreads();
+  G::sync();
   if (tid == 0) {
     int32_t* counts = p.seg_counts + ((int64_t)r * P + seg) * 2;
-    counts[0] = (int32_t)st.seg_c0;
-    counts[1] = (int32_t)st.seg_cb;
+    counts[0] = (int32_t)sl.seg_c0;
+    counts[1] = (int32_t)sl.seg_cb;
     __threadfence();
     const int prev = atomicAdd(p.counters + kCtrArriveBase + r, 1);
-    st.is_last = prev == P - 1;
+    sl.is_last = prev == P - 1;
   }
-  __syncthreads();
-  if (!st.is_last) return;
+  G::sync();
+  if (!sl.is_last) return;
 
   // ---- finisher: merge (eq. 27), certify, refine or recover ----
   __threadfence();
   if (tid == 0) atomicExch(p.counters + kCtrArriveBase + r, 0);
   for (int q = tid; q < P; q += kKvSplitThreads) {
     const int32_t* cq = p.seg_counts + ((int64_t)r * P + q) * 2;
-    st.run_c0[q] = (uint32_t)__ldcg(cq);
-    st.run_cb[q] = (uint32_t)__ldcg(cq + 1);
+    run_c0[q] = (uint32_t)__ldcg(cq);
+    run_cb[q] = (uint32_t)__ldcg(cq + 1);
   }
-  __syncthreads();
+  G::sync();
   if (tid < 32) {
     // Totals of both counts, each lane summing up to 4 consecutive segments.
     uint32_t s0 = 0u, sb = 0u;
     for (int q = tid * 4; q < tid * 4 + 4 && q < P; ++q) {
-      s0 += st.run_c0[q];
-      sb += st.run_cb[q];
+      s0 += run_c0[q];
+      sb += run_cb[q];
     }
     s0 = __reduce_add_sync(kFull, s0);
     sb = __reduce_add_sync(kFull, sb);
     if (tid == 0) {
-      st.tot_c0 = s0;
-      st.tot_cb = sb;
+      sl.c0 = (int)s0;
+      sl.c1 = (int)sb;
     }
   }
-  __syncthreads();
-  const uint32_t c0 = st.tot_c0, cb = st.tot_cb;
+  G::sync();
+  const uint32_t c0 = (uint32_t)sl.c0, cb = (uint32_t)sl.c1;
   int route;
   bool certified;
   bool with_band = false;
@@ -1376,18 +1460,18 @@ __global__ void __launch_bounds__(kKvSplitThreads, ETK_SAMPLED_MIN_CTAS) kv_spli
     if (tid == 0) {
       uint32_t acc = 0u;
       for (int q = 0; q < P; ++q) {
-        st.run_pre[q] = acc;
-        acc += st.run_c0[q] + (with_band ? st.run_cb[q] : 0u);
+        run_pre[q] = acc;
+        acc += run_c0[q] + (with_band ? run_cb[q] : 0u);
       }
-      st.run_pre[P] = acc;
+      run_pre[P] = acc;
     }
-    clear_hist<kKvSplitThreads>(st, 2048);
-    __syncthreads();
+    clear_hist<G>(hist, 2048);
+    G::sync();
     // Gather the runs into the frontier in order.  Logical position f maps to
     // shared memory below cap and to rb[f] above; every source position is >=
     // its logical position, so gathering in chunks (read all, then write)
     // never overwrites an unread entry.
-    const uint32_t total = st.run_pre[P];
+    const uint32_t total = run_pre[P];
     constexpr int R = 4;
     constexpr uint32_t CH = kKvSplitThreads * R;
     for (uint32_t c = 0; c < total; c += CH) {
@@ -1401,7 +1485,7 @@ __global__ void __launch_bounds__(kKvSplitThreads, ETK_SAMPLED_MIN_CTAS) kv_spli
           int lo_q = 0, hi_q = P - 1;  // last q with run_pre[q] <= g
           while (lo_q < hi_q) {
             const int mid = (lo_q + hi_q + 1) >> 1;
-            if (st.run_pre[mid] <= g)
+            if (run_pre[mid] <= g)
               lo_q = mid;
             else
               hi_q = mid - 1;
@@ -1409,33 +1493,36 @@ __global__ void __launch_bounds__(kKvSplitThreads, ETK_SAMPLED_MIN_CTAS) kv_spli
           const int q = lo_q;
           int slo, shi;
           segment_bounds(L, P, q, slo, shi);
-          const uint32_t off = g - st.run_pre[q];
-          const uint32_t n0 = st.run_c0[q];
+          const uint32_t off = g - run_pre[q];
+          const uint32_t n0 = run_c0[q];
           // band entries occupy [shi - nb, shi); read them in ascending order
           // so that every source position is >= its logical position
-          const int src = off < n0 ? slo + (int)off
-                                   : shi - (int)st.run_cb[q] + (int)(off - n0);
+          const int src = off < n0 ? slo + (int)off : shi - (int)run_cb[q] + (int)(off - n0);
           const uint2 e = __ldcg(rb + src);
           idx[k] = (int32_t)e.x;
           key[k] = e.y;
         }
       }
-      __syncthreads();
+      G::sync();
 #pragma unroll
       for (int k = 0; k < R; ++k) {
         if (idx[k] == -2) continue;
         F.put(c + k * kKvSplitThreads + tid, idx[k], key[k]);
-        atomicAdd(&st.hist[key[k] >> 21], 1u);
+        atomicAdd(&hist[key[k] >> 21], 1u);
       }
-      __syncthreads();
+      G::sync();
     }
     q0n = (int)total;
-    refine<kKvSplitThreads>(F, total, (uint32_t)K, st, out_row, K);
+    refine<G>(F, total, (uint32_t)K, hist, sc, sl, out_row, K);
   } else {
-    exact_route<kKvSplitThreads>(p, row, L, F, st, out_row, tstar, e0, q0n);
+    exact_recovery<G>(p, row, L, F, hist, sc, sl, out_row, queues);
+    tstar = sl.tstar;
+    e0 = sl.e0;
+    q0n = sl.q0n;
+    refine<G>(F, sl.n_front, (uint32_t)(K - e0), hist, sc, sl, out_row, K);
   }
-  finish_row<kKvSplitThreads>(p, st, out_row);
-  write_trace(p, r, route, tau0, guess ? -1 : tau1, (int)c0, c1, tstar, e0, q0n);
+  finish_row<G>(p, sl, out_row);
+  if (tid == 0) write_trace(p, r, route, tau0, tau1, (int)c0, c1, tstar, e0, q0n);
 }
 
 // Kernel attributes are set once per (device, kernel); later launches, which
@@ -1461,12 +1548,7 @@ int set_attrs(KernelT kernel, int family, size_t smem) {
 
 }  // namespace
 
-size_t shared_bytes(int family, int cap) {
-  const int threads =
-      family == EXACT_TOPK_FAMILY_ROW_LOCAL_EXACT ? kRowLocalThreads : kPersistentThreads;
-  return sizeof(RowState) + (size_t)cap * sizeof(uint2) +
-         (size_t)(threads / 32) * kQueueWords * sizeof(uint32_t);
-}
+size_t shared_bytes(int family, int cap) { return smem_layout(family, cap).total; }
 
 int kernel_occupancy(int family, int device, int* ctas_per_sm) {
   int prev = 0;
@@ -1556,7 +1638,6 @@ int launch(const exact_topk_plan& plan, const LaunchArgs& a, cudaStream_t stream
 }
 
 }  // namespace etk
-
 
 // ----------------------------------------------------------------------------
 // Allocation-free entry point
