@@ -172,6 +172,26 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
   return m;
 }
 
+// Per-thread run-length merging of histogram increments: consecutive adds to
+// the same bin become one shared atomic.  Rows of few distinct values
+// (constant rows, tie bands, signed zeros) would otherwise put every lane of a
+// warp on one shared address.
+struct RunHist {
+  uint32_t bin = 0u, cnt = 0u;
+  __device__ __forceinline__ void add(uint32_t* hist, uint32_t b) {
+    if (cnt != 0u && b != bin) {
+      atomicAdd(&hist[bin], cnt);
+      cnt = 0u;
+    }
+    bin = b;
+    ++cnt;
+  }
+  __device__ __forceinline__ void flush(uint32_t* hist) {
+    if (cnt != 0u) atomicAdd(&hist[bin], cnt);
+    cnt = 0u;
+  }
+};
+
 // ----------------------------------------------------------------------------
 // Loads
 // ----------------------------------------------------------------------------
@@ -265,6 +285,9 @@ struct Params {
 // capacity gcap (section 5.4: "Two global ping-pong slices extend the shared
 // frontier"; here one slice per row slot suffices because compaction is done
 // in place).  Entries are (index, key) pairs stored together.
+constexpr int kRefineBatch = 8;  // frontier entries per thread in flight in Phase 3 histograms
+constexpr int kCommitBatch = 4;  // ... and in its final commit pass
+
 struct Frontier {
   uint2* s;
   uint32_t cap;
@@ -510,6 +533,8 @@ __device__ __forceinline__ void drain_queue(const WarpQueue& q, int n, int a0, i
         sinkB(pB++, ibase + e, d);
     }
   }
+  sinkA.count8(mA, u);
+  sinkB.count8(mB, u);
 }
 
 // One pass of group G over row[lo, hi) that classifies every score by its
@@ -540,10 +565,13 @@ __device__ __forceinline__ void scan_tiles(const float* row, int lo, int hi, uin
     const int i = tid < head ? lo + tid : sp.a_end + (tid - head);
     const uint32_t d = desc_key(ld_stream1(row + i));
     if (d <= TB) {
-      if (A_ON && d <= TA)
+      if (A_ON && d <= TA) {
         sinkA(atomicAdd(cntA, 1u), i, d);
-      else
+        sinkA.count1(d);
+      } else {
         sinkB(atomicAdd(cntB, 1u), i, d);
+        sinkB.count1(d);
+      }
     }
   }
   const int CB = (int)bits_from_desc(TB);
@@ -665,17 +693,25 @@ __device__ void scan_coarse_hist(const float* row, int lo, int hi, uint32_t* his
     const bool second = t + G::kThreads < sp.nvec;
     ld_stream8(body + 8 * t, x);
     if (second) ld_stream8(body + 8 * (t + G::kThreads), x + 8);
+    RunHist rh;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) atomicAdd(&hist[coarse_bin(x[k])], 1u);
+    for (int k = 0; k < 8; ++k) rh.add(hist, (uint32_t)coarse_bin(x[k]));
     if (second) {
 #pragma unroll
-      for (int k = 8; k < 16; ++k) atomicAdd(&hist[coarse_bin(x[k])], 1u);
+      for (int k = 8; k < 16; ++k) rh.add(hist, (uint32_t)coarse_bin(x[k]));
     }
+    rh.flush(hist);
   }
 }
 
 // Sinks: where an admitted (position, index, key) goes.
-struct FrontierSink {  // frontier entry + leading-digit histogram (eqs. 17, 20)
+// operator() stores one entry; count8 (the keys of u[e] for the bits e of m)
+// and count1 feed the sink's histogram, if it has one.
+struct NoCount {
+  __device__ __forceinline__ void count8(uint32_t, const uint32_t*) const {}
+  __device__ __forceinline__ void count1(uint32_t) const {}
+};
+struct FrontierSink : NoCount {  // frontier entry + leading-digit histogram (eqs. 17, 20)
   Frontier F;
   uint32_t* hist;
   __device__ __forceinline__ void operator()(uint32_t p, int32_t i, uint32_t d) const {
@@ -683,14 +719,14 @@ struct FrontierSink {  // frontier entry + leading-digit histogram (eqs. 17, 20)
     atomicAdd(&hist[d >> 21], 1u);
   }
 };
-struct CommitSink {  // committed straight to the output (E0 of eq. 20)
+struct CommitSink : NoCount {  // committed straight to the output (E0 of eq. 20)
   int32_t* out_row;
   uint32_t K;
   __device__ __forceinline__ void operator()(uint32_t p, int32_t i, uint32_t) const {
     if (p < K) out_row[p] = i;
   }
 };
-struct DropSink {
+struct DropSink : NoCount {
   __device__ __forceinline__ void operator()(uint32_t, int32_t, uint32_t) const {}
 };
 
@@ -764,33 +800,58 @@ __device__ void refine(const Frontier& F, uint32_t n, uint32_t k, uint32_t* hist
     G::sync();  // the finder is done with hist
     clear_hist<G>(hist, 2048);
     G::sync();
-    for (uint32_t p = tid; p < n; p += G::kThreads) {
-      int32_t i;
-      uint32_t d;
-      F.get(p, i, d);
-      if ((d >> shift) == prefix) atomicAdd(&hist[digit(d, j + 1)], 1u);
+    // Eight entries per thread in flight (the frontier may live in global
+    // memory), then run-length merged histogram adds.
+    for (uint32_t p0 = 0; p0 < n; p0 += kRefineBatch * G::kThreads) {
+      uint32_t d[kRefineBatch];
+#pragma unroll
+      for (int b = 0; b < kRefineBatch; ++b) {
+        const uint32_t pp = p0 + b * G::kThreads + tid;
+        int32_t i;
+        d[b] = 0xFFFFFFFFu;
+        if (pp < n) F.get(pp, i, d[b]);
+      }
+      RunHist rh;
+#pragma unroll
+      for (int b = 0; b < kRefineBatch; ++b) {
+        const uint32_t pp = p0 + b * G::kThreads + tid;
+        if (pp < n && (d[b] >> shift) == prefix) rh.add(hist, digit(d[b], j + 1));
+      }
+      rh.flush(hist);
     }
     G::sync();
   }
   if (resolved) {
     if (tid == 0) sl.n_keep = 0u;
     G::sync();
-    for (uint32_t p = tid; p < nr; p += G::kThreads) {
-      int32_t i = -1;
-      uint32_t d = 0xFFFFFFFFu;
-      if (p < n) F.get(p, i, d);
-      const bool in = p < n;
-      const bool com = in && (uint64_t)d < commit_below;
-      const bool tie = in && ties > 0u && d == tie_key;
-      const uint32_t tb = __ballot_sync(kFull, tie);
-      bool take = false;
-      if (tb) {
-        uint32_t base = 0u;
-        if ((threadIdx.x & 31) == 0) base = atomicAdd(&sl.n_keep, (uint32_t)__popc(tb));
-        base = __shfl_sync(kFull, base, 0);
-        take = tie && base + (uint32_t)__popc(tb & lt) < ties;
+    for (uint32_t p0 = 0; p0 < nr; p0 += kCommitBatch * G::kThreads) {
+      int32_t ib[kCommitBatch];
+      uint32_t db[kCommitBatch];
+#pragma unroll
+      for (int b = 0; b < kCommitBatch; ++b) {
+        const uint32_t pp = p0 + b * G::kThreads + tid;
+        ib[b] = -1;
+        db[b] = 0xFFFFFFFFu;
+        if (pp < n) F.get(pp, ib[b], db[b]);
       }
-      commit_warp(&sl.n_out, out_row, K, com || take, i, lt);
+#pragma unroll
+      for (int b = 0; b < kCommitBatch; ++b) {
+        const uint32_t pp = p0 + b * G::kThreads + tid;
+        if (p0 + b * G::kThreads >= nr) break;  // warp-uniform: nr and the stride are multiples of 32
+        const bool in = pp < n;
+        const uint32_t d = db[b];
+        const bool com = in && (uint64_t)d < commit_below;
+        const bool tie = in && ties > 0u && d == tie_key;
+        const uint32_t tb = __ballot_sync(kFull, tie);
+        bool take = false;
+        if (tb) {
+          uint32_t base = 0u;
+          if ((threadIdx.x & 31) == 0) base = atomicAdd(&sl.n_keep, (uint32_t)__popc(tb));
+          base = __shfl_sync(kFull, base, 0);
+          take = tie && base + (uint32_t)__popc(tb & lt) < ties;
+        }
+        commit_warp(&sl.n_out, out_row, K, com || take, ib[b], lt);
+      }
     }
   }
   G::sync();
@@ -875,8 +936,8 @@ __device__ void exact_recovery(const Params& p, const float* row, int L, const F
   const uint32_t tlo = sl.T0, thi = sl.T1;
   clear_hist<G>(hist, 2048);
   G::sync();
-  CommitSink commit_sink{out_row, (uint32_t)K};
-  FrontierSink front_sink{F, hist};
+  CommitSink commit_sink{{}, out_row, (uint32_t)K};
+  FrontierSink front_sink{{}, F, hist};
   scan_two_class<G>(row, 0, L, tlo, thi, tstar > 0, &sl.n_out, &sl.n_front, queues, commit_sink,
                     front_sink);
   G::sync();
@@ -916,13 +977,17 @@ __device__ void exact_recovery_resident(const Params& p, const float* row, int L
     sl.n_out = 0u;
   }
   G::sync();
+  {
+    RunHist rh;
 #pragma unroll
-  for (int g = 0; g < VPT / 8; ++g) {
+    for (int g = 0; g < VPT / 8; ++g) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int i = (g * G::kThreads + tid) * 8 + e;
-      if (i < L) atomicAdd(&hist[coarse_bin(v[g * 8 + e])], 1u);
+      for (int e = 0; e < 8; ++e) {
+        const int i = (g * G::kThreads + tid) * 8 + e;
+        if (i < L) rh.add(hist, (uint32_t)coarse_bin(v[g * 8 + e]));
+      }
     }
+    rh.flush(hist);
   }
   G::sync();
   find_boundaries<G>(hist, sc, 2048, 1, (uint32_t)K, 0u);
@@ -942,10 +1007,16 @@ __device__ void exact_recovery_resident(const Params& p, const float* row, int L
       const bool valid = i < L && d <= thi;
       const bool com = valid && has_lo && d <= tlo;
       commit_warp(&sl.n_out, out_row, K, com, i, lt);
-      if (valid && !com) {
-        const uint32_t q = atomicAdd(&sl.n_front, 1u);
-        F.put(q, i, d);
-        atomicAdd(&hist[d >> 21], 1u);
+      const bool keep = valid && !com;
+      const uint32_t kb = __ballot_sync(kFull, keep);
+      if (kb != 0u) {
+        uint32_t base = 0u;
+        if ((tid & 31) == 0) base = atomicAdd(&sl.n_front, (uint32_t)__popc(kb));
+        base = __shfl_sync(kFull, base, 0);
+        if (keep) {
+          F.put(base + (uint32_t)__popc(kb & lt), i, d);
+          atomicAdd(&hist[d >> 21], 1u);
+        }
       }
     }
   }
@@ -1159,7 +1230,7 @@ __device__ void simple_row(const Params& p, int r, Slot& sl, const Frontier& F, 
     sl.e0 = 0;
   }
   G::sync();
-  FrontierSink front_sink{F, hist};
+  FrontierSink front_sink{{}, F, hist};
   DropSink drop;
   bool exact = false;
   int route;
@@ -1299,14 +1370,14 @@ __device__ __forceinline__ void segment_bounds(int L, int P, int p, int& lo, int
 
 // Segment candidate sinks: primary entries fill the segment's range of the row
 // buffer from its start, band entries from its end.
-struct SegmentFrontSink {
+struct SegmentFrontSink : NoCount {
   uint2* rb;
   int lo;
   __device__ __forceinline__ void operator()(uint32_t p, int32_t i, uint32_t d) const {
     rb[lo + (int)p] = make_uint2((uint32_t)i, d);
   }
 };
-struct SegmentBackSink {
+struct SegmentBackSink : NoCount {
   uint2* rb;
   int hi;
   __device__ __forceinline__ void operator()(uint32_t p, int32_t i, uint32_t d) const {
@@ -1392,8 +1463,8 @@ __global__ void __launch_bounds__(kKvSplitThreads, 2) kv_split_kernel(Params p) 
   int lo, hi;
   segment_bounds(L, P, seg, lo, hi);
   {
-    SegmentFrontSink primary{rb, lo};
-    SegmentBackSink band{rb, hi};
+    SegmentFrontSink primary{{}, rb, lo};
+    SegmentBackSink band{{}, rb, hi};
     scan_two_class<G>(row, lo, hi, T0, use_band ? T1 : T0, true, &sl.seg_c0, &sl.seg_cb, queues,
                       primary, band);
   }
