@@ -42,7 +42,8 @@ MEASURED_PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
 PROFILES = os.path.join(ROOT, "profiles")
 KERNEL_SOURCE = os.path.join(ROOT, "exact_top_selection_gb300", "csrc", "topk_kernels.cu")
-KERNEL_NAMES = {1: "persistent_sampled_kernel", 2: "kv_split_kernel", 3: "row_local_exact_kernel"}
+KERNEL_NAMES = {1: "persistent_sampled_kernel", 2: "kv_split_kernel", 3: "row_local_exact_kernel",
+                4: "cluster_split_kernel"}
 
 
 # ---------------------------------------------------------------- distributed helpers

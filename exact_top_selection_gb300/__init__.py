@@ -25,14 +25,15 @@ __all__ = [
     "DeviceInfo", "Plan", "PlanRequest", "ExactTopK", "ExactTopKError",
     "library", "library_path", "query_device", "make_plan", "workspace_size", "topk", "run",
     "error_string", "version", "FAMILY_AUTO", "FAMILY_PERSISTENT_SAMPLED", "FAMILY_KV_SPLIT",
-    "FAMILY_ROW_LOCAL_EXACT", "TRACE_FIELDS", "ROUTES", "EXPORTED_SYMBOLS",
+    "FAMILY_ROW_LOCAL_EXACT", "FAMILY_CLUSTER_SPLIT", "TRACE_FIELDS", "ROUTES", "EXPORTED_SYMBOLS",
 ]
 
 FAMILY_AUTO = 0
 FAMILY_PERSISTENT_SAMPLED = 1
 FAMILY_KV_SPLIT = 2
 FAMILY_ROW_LOCAL_EXACT = 3
-FAMILY_NAMES = {1: "persistent_sampled", 2: "kv_split", 3: "row_local_exact"}
+FAMILY_CLUSTER_SPLIT = 4
+FAMILY_NAMES = {1: "persistent_sampled", 2: "kv_split", 3: "row_local_exact", 4: "cluster_split"}
 
 ROUTES = ("pad", "primary", "band", "exact_after_band", "exact_no_band", "direct_exact", "guess",
           "guess_exact")
@@ -51,7 +52,8 @@ class ExactTopKError(RuntimeError):
 
 class DeviceInfo(ctypes.Structure):
     _fields_ = [("sm_count", ctypes.c_int32), ("persistent_ctas_per_sm", ctypes.c_int32),
-                ("kvsplit_ctas_per_sm", ctypes.c_int32), ("rowlocal_ctas_per_sm", ctypes.c_int32)]
+                ("kvsplit_ctas_per_sm", ctypes.c_int32), ("rowlocal_ctas_per_sm", ctypes.c_int32),
+                ("cluster_ctas_per_sm", ctypes.c_int32)]
 
 
 class PlanRequest(ctypes.Structure):

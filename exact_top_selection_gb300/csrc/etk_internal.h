@@ -23,6 +23,11 @@ constexpr int kCtrArriveBase = 4;
 constexpr int kPersistentThreads = 512;
 constexpr int kKvSplitThreads = 512;
 constexpr int kRowLocalThreads = 1024;
+constexpr int kClusterThreads = 512;
+// Scores of one row segment resident in a cluster CTA's shared memory, and
+// the largest cluster (the portable limit).
+constexpr int kClusterStage = 16384;
+constexpr int kClusterMaxSplits = 8;
 constexpr int kPersistentCap = 4096;
 constexpr int kKvSplitCap = 4096;
 constexpr int kRowLocalCap = 8192;

@@ -124,6 +124,8 @@ int exact_topk_query_device(int device, exact_topk_device_info* info) {
   if (rc != EXACT_TOPK_OK) return rc;
   rc = kernel_occupancy(EXACT_TOPK_FAMILY_ROW_LOCAL_EXACT, device, &d.rowlocal_ctas_per_sm);
   if (rc != EXACT_TOPK_OK) return rc;
+  rc = kernel_occupancy(EXACT_TOPK_FAMILY_CLUSTER_SPLIT, device, &d.cluster_ctas_per_sm);
+  if (rc != EXACT_TOPK_OK) return rc;
   *info = d;
   return EXACT_TOPK_OK;
 }
@@ -150,18 +152,23 @@ int exact_topk_make_plan(int64_t num_rows, int64_t max_kv_len, int64_t row_pitch
 
   // Family (section 5.5, Fig. 6): row-local exact below the sampling
   // crossover (section 6.4: exact proposals win at 16-24K columns, sampling
-  // wins at 64K), KV-split when rows cannot fill the device, persistent
-  // sampled otherwise.
+  // wins at 64K); when rows cannot fill the device, the cluster split if a
+  // row fits the shared memory of one cluster (and its CTAs fit in about
+  // two waves), else the KV-split; persistent sampled otherwise.
+  const int64_t cluster_P = ceil_div64(max_kv_len, kClusterStage);
   int family = r.family;
   if (family == EXACT_TOPK_FAMILY_AUTO) {
     if (max_kv_len < 32768)
       family = EXACT_TOPK_FAMILY_ROW_LOCAL_EXACT;
     else if (num_rows < info->sm_count)
-      family = EXACT_TOPK_FAMILY_KV_SPLIT;
+      family = (cluster_P <= kClusterMaxSplits && info->cluster_ctas_per_sm > 0 &&
+                num_rows * cluster_P <= 2LL * info->sm_count * info->cluster_ctas_per_sm)
+                   ? EXACT_TOPK_FAMILY_CLUSTER_SPLIT
+                   : EXACT_TOPK_FAMILY_KV_SPLIT;
     else
       family = EXACT_TOPK_FAMILY_PERSISTENT_SAMPLED;
   }
-  if (family < EXACT_TOPK_FAMILY_PERSISTENT_SAMPLED || family > EXACT_TOPK_FAMILY_ROW_LOCAL_EXACT)
+  if (family < EXACT_TOPK_FAMILY_PERSISTENT_SAMPLED || family > EXACT_TOPK_FAMILY_CLUSTER_SPLIT)
     return EXACT_TOPK_ERR_BAD_PLAN;
   p.family = family;
 
@@ -197,6 +204,11 @@ int exact_topk_make_plan(int64_t num_rows, int64_t max_kv_len, int64_t row_pitch
       p.cand_capacity = kKvSplitCap;
       ctas_per_sm = info->kvsplit_ctas_per_sm;
       break;
+    case EXACT_TOPK_FAMILY_CLUSTER_SPLIT:
+      p.threads = kClusterThreads;
+      p.cand_capacity = kClusterStage;
+      ctas_per_sm = info->cluster_ctas_per_sm;
+      break;
     default:
       p.threads = kRowLocalThreads;
       p.cand_capacity = kRowLocalCap;
@@ -217,6 +229,12 @@ int exact_topk_make_plan(int64_t num_rows, int64_t max_kv_len, int64_t row_pitch
       while (P > 1 && max_kv_len / P < 8192) P /= 2;
     }
     if (P < 1 || P > 128 || num_rows > 65535) return EXACT_TOPK_ERR_BAD_PLAN;
+    p.splits = (int32_t)P;
+    p.workers = (int32_t)(num_rows * P);
+  } else if (family == EXACT_TOPK_FAMILY_CLUSTER_SPLIT) {
+    // The fewest CTAs whose shared memory holds the widest row.
+    const int64_t P = r.splits ? r.splits : cluster_P;
+    if (P < cluster_P || P > kClusterMaxSplits || num_rows > 65535) return EXACT_TOPK_ERR_BAD_PLAN;
     p.splits = (int32_t)P;
     p.workers = (int32_t)(num_rows * P);
   } else {
@@ -262,7 +280,7 @@ int exact_topk_run(const exact_topk_plan* plan, const float* logits, const int32
     return EXACT_TOPK_ERR_BAD_SHAPE;
   if (plan->top_k < 1 || plan->top_k > EXACT_TOPK_MAX_K) return EXACT_TOPK_ERR_BAD_K;
   if (plan->family < EXACT_TOPK_FAMILY_PERSISTENT_SAMPLED ||
-      plan->family > EXACT_TOPK_FAMILY_ROW_LOCAL_EXACT || plan->workers < 1 ||
+      plan->family > EXACT_TOPK_FAMILY_CLUSTER_SPLIT || plan->workers < 1 ||
       plan->splits < 1 || plan->stride < 2 || !is_pow2(plan->stride) || plan->q0 < 1 ||
       plan->q1 < 1 || (plan->dual != 0 && plan->dual != 1))
     return EXACT_TOPK_ERR_BAD_PLAN;
@@ -270,10 +288,18 @@ int exact_topk_run(const exact_topk_plan* plan, const float* logits, const int32
       (plan->num_rows > 65535 || plan->splits > 128 ||
        (int64_t)plan->workers != plan->num_rows * plan->splits))
     return EXACT_TOPK_ERR_BAD_PLAN;
+  if (plan->family == EXACT_TOPK_FAMILY_CLUSTER_SPLIT &&
+      (plan->num_rows > 65535 || plan->splits > kClusterMaxSplits ||
+       (int64_t)plan->splits * kClusterStage < plan->max_kv_len ||
+       (int64_t)plan->workers != plan->num_rows * plan->splits))
+    return EXACT_TOPK_ERR_BAD_PLAN;
   const int expect_cap = plan->family == EXACT_TOPK_FAMILY_PERSISTENT_SAMPLED
                              ? kPersistentCap
-                             : (plan->family == EXACT_TOPK_FAMILY_KV_SPLIT ? kKvSplitCap
-                                                                           : kRowLocalCap);
+                             : (plan->family == EXACT_TOPK_FAMILY_KV_SPLIT
+                                    ? kKvSplitCap
+                                    : (plan->family == EXACT_TOPK_FAMILY_CLUSTER_SPLIT
+                                           ? kClusterStage
+                                           : kRowLocalCap));
   if (plan->cand_capacity != expect_cap) return EXACT_TOPK_ERR_BAD_PLAN;
   const WorkspaceLayout lay = workspace_layout(*plan);
   if (lay.total != plan->workspace_bytes) return EXACT_TOPK_ERR_BAD_PLAN;

@@ -13,6 +13,9 @@
 //   row_local_exact_kernel     one 1024-thread CTA per row takes the exact
 //                              coarse route directly; short rows stay in
 //                              registers between the two classification passes.
+//   cluster_split_kernel       the P CTAs of one thread-block cluster hold one
+//                              row in shared memory (TMA bulk copies) and merge
+//                              through distributed shared memory.
 //
 // Every route ends in the same refinement interface (E0, Q0, k0, h0) of eqs.
 // 20-21 and the 11+11+10 prefix-commit-retain recurrence of eqs. 22-25.
@@ -60,6 +63,7 @@ template <int THREADS>
 struct CtaGroup {
   static constexpr int kThreads = THREADS;
   static constexpr int kWarps = THREADS / 32;
+  static_assert(THREADS % 32 == 0 && kWarps <= 32, "whole warps, at most 32");
   __device__ __forceinline__ static int rank() { return (int)threadIdx.x; }
   __device__ __forceinline__ static void sync() { __syncthreads(); }
 };
@@ -376,61 +380,83 @@ __device__ __forceinline__ void clear_hist(uint32_t* hist, int nbins) {
 // inclusive prefix H of hist[0, nbins), res_below = H(b - 1) and res_cnt =
 // hist[b]; res_bin = -1 (res_below = total) when the total is below t.  The
 // histogram is only read.  Entered by the whole group after the histogram is
-// complete, with a group barrier between consecutive calls (results of a call
-// are written exactly once, by the thread owning the boundary bin or by the
-// last thread); results are visible to every thread of the group on return.
+// complete, with a group barrier between consecutive calls; results are
+// visible to every thread of the group on return.
+//
+// nbins is a multiple of 128 with at most one 128-bin chunk per warp: warp w
+// sums chunk w (lane l holds its bins 4l .. 4l+3), and after one barrier every
+// warp scans the chunk totals, so that the warp whose chunk holds a target
+// resolves it from the registers it already has.
 template <class G>
 __device__ void find_boundaries(const uint32_t* hist, GroupScratch& sc, int nbins, int ntargets,
                                 uint32_t t0, uint32_t t1) {
-  constexpr int kWarps = G::kWarps;
   const int tid = G::rank(), lane = tid & 31, warp = tid >> 5;
-  const int per = (nbins + G::kThreads - 1) / G::kThreads;
-  const int b0 = tid * per;
-  uint32_t local = 0;
-  for (int k = 0; k < per; ++k) local += b0 + k < nbins ? hist[b0 + k] : 0u;
-  uint32_t incl = local;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t v = __shfl_up_sync(kFull, incl, o);
-    if (lane >= o) incl += v;
+  const int nch = nbins >> 7;
+  uint4 v = make_uint4(0u, 0u, 0u, 0u);
+  uint32_t s4 = 0u;
+  if (warp < nch) {
+    v = reinterpret_cast<const uint4*>(hist)[warp * 32 + lane];
+    s4 = v.x + v.y + v.z + v.w;
+    const uint32_t tot = __reduce_add_sync(kFull, s4);
+    if (lane == 0) sc.warp_sums[warp] = tot;
   }
-  if (lane == 31) sc.warp_sums[warp] = incl;
   G::sync();
-  // Every warp scans the warp totals itself (no second barrier).
-  uint32_t w = lane < kWarps ? sc.warp_sums[lane] : 0u;
+  if (warp < nch) {
+    const uint32_t ct = lane < nch ? sc.warp_sums[lane] : 0u;
+    uint32_t cincl = ct;  // inclusive prefix over chunks
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t v = __shfl_up_sync(kFull, w, o);
-    if (lane >= o) w += v;
-  }
-  const uint32_t before_warp = warp ? __shfl_sync(kFull, w, warp - 1) : 0u;
-  const uint32_t grand = __shfl_sync(kFull, w, kWarps - 1);
-  uint32_t run = before_warp + (incl - local);
-  for (int k = 0; k < per; ++k) {
-    const uint32_t h = b0 + k < nbins ? hist[b0 + k] : 0u;
-    const uint32_t prev = run;
-    run += h;
-    if (prev < t0 && t0 <= run) {
-      sc.res_bin[0] = b0 + k;
-      sc.res_below[0] = prev;
-      sc.res_cnt[0] = h;
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFull, cincl, o);
+      if (lane >= o) cincl += y;
     }
-    if (ntargets > 1 && prev < t1 && t1 <= run) {
-      sc.res_bin[1] = b0 + k;
-      sc.res_below[1] = prev;
-      sc.res_cnt[1] = h;
+    const uint32_t grand = __shfl_sync(kFull, cincl, 31);
+    const uint32_t mine_before = __shfl_sync(kFull, cincl - ct, warp);  // before chunk `warp`
+    uint32_t incl = s4;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += y;
     }
-  }
-  if (tid == G::kThreads - 1) {
-    if (grand < t0) {
-      sc.res_bin[0] = -1;
-      sc.res_below[0] = grand;
-      sc.res_cnt[0] = 0u;
-    }
-    if (ntargets > 1 && grand < t1) {
-      sc.res_bin[1] = -1;
-      sc.res_below[1] = grand;
-      sc.res_cnt[1] = 0u;
+    const uint32_t excl = mine_before + incl - s4;
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      if (x >= ntargets) break;
+      const uint32_t t = x == 0 ? t0 : t1;
+      if (grand < t) {
+        if (warp == 0 && lane == 0) {
+          sc.res_bin[x] = -1;
+          sc.res_below[x] = grand;
+          sc.res_cnt[x] = 0u;
+        }
+        continue;
+      }
+      if (t == 0u) {  // H(0) >= 0
+        if (warp == 0 && lane == 0) {
+          sc.res_bin[x] = 0;
+          sc.res_below[x] = 0u;
+          sc.res_cnt[x] = hist[0];
+        }
+        continue;
+      }
+      // the lane (of the chunk's warp) whose four bins cross t
+      if (excl < t && t <= excl + s4) {
+        const uint32_t h[4] = {v.x, v.y, v.z, v.w};
+        uint32_t r0 = excl;
+        int b = -1;
+        uint32_t bl = 0u, bc = 0u;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (b < 0 && r0 + h[i] >= t) {
+            b = i;
+            bl = r0;
+            bc = h[i];
+          }
+          r0 += h[i];
+        }
+        sc.res_bin[x] = warp * 128 + lane * 4 + b;
+        sc.res_below[x] = bl;
+        sc.res_cnt[x] = bc;
+      }
     }
   }
   G::sync();
@@ -1038,6 +1064,32 @@ __device__ __forceinline__ int view_size(int L, int a, int s) {
   return L > a ? (L - a + s - 1) / s : 0;
 }
 
+// Boundaries tau0 / tau1 of a complete view histogram (eq. 15: the first bins
+// whose inclusive prefix reaches q0 / q1) and their inclusive cutoffs (section
+// 4.3), written to the slot.
+template <class G>
+__device__ void view_cutoffs(const Params& p, const uint32_t* hist, GroupScratch& sc, Slot& sl) {
+  find_boundaries<G>(hist, sc, 2048, p.dual ? 2 : 1, (uint32_t)p.q0, (uint32_t)p.q1);
+  const int warp = G::rank() >> 5;
+  if (warp == 0 || (warp == 1 && p.dual)) {
+    const int b = sc.res_bin[warp];
+    const uint32_t t = cutoff_fast_warp(b);
+    if ((G::rank() & 31) == 0) {
+      if (warp == 0) {
+        sl.T0 = t;
+        sl.tau0 = b;
+      } else {
+        sl.T1 = t;
+        sl.tau1 = b;
+      }
+    }
+  } else if (warp == 1 && G::rank() == 32) {
+    sl.T1 = 0u;
+    sl.tau1 = -1;
+  }
+  G::sync();
+}
+
 // Phase 1 (section 4.2, eqs. 13-15) by group G: coarse histogram of the view
 // V = {i < L : i = a_r (mod s)}, the boundaries tau0 / tau1 and their
 // inclusive cutoffs, written to the slot.  Each thread issues up to 8 view
@@ -1066,22 +1118,7 @@ __device__ void sample_view(const Params& p, const float* row, int L, int a, uin
       if (t0 + k * G::kThreads + tid < nv) atomicAdd(&hist[coarse_bin(u[k])], 1u);
   }
   G::sync();
-  find_boundaries<G>(hist, sc, 2048, 2, (uint32_t)p.q0, (uint32_t)p.q1);
-  const int warp = tid >> 5;
-  if (warp == 0) {
-    const uint32_t t = cutoff_fast_warp(sc.res_bin[0]);
-    if ((tid & 31) == 0) {
-      sl.T0 = t;
-      sl.tau0 = sc.res_bin[0];
-    }
-  } else if (warp == 1) {
-    const uint32_t t = p.dual ? cutoff_fast_warp(sc.res_bin[1]) : 0u;
-    if ((tid & 31) == 0) {
-      sl.T1 = t;
-      sl.tau1 = p.dual ? sc.res_bin[1] : -1;
-    }
-  }
-  G::sync();
+  view_cutoffs<G>(p, hist, sc, sl);
 }
 
 // Optional guess source (previous-step Top-K): the worst coarse bin of the K
@@ -1596,10 +1633,826 @@ __global__ void __launch_bounds__(kKvSplitThreads, 2) kv_split_kernel(Params p) 
   if (tid == 0) write_trace(p, r, route, tau0, tau1, (int)c0, c1, tstar, e0, q0n);
 }
 
+// ----------------------------------------------------------------------------
+// Kernel 4: cluster-resident split (section 4.5 eqs. 26-27, merge made on chip)
+// ----------------------------------------------------------------------------
+//
+// The P CTAs of one thread-block cluster own one row.  Each CTA copies its
+// segment (at most kClusterStage scores) into shared memory with one TMA bulk
+// copy, issued right after the loads of the replicated Phase-1 view so that
+// the copy overlaps the view.  Phase 2 is one pass over the resident segment
+// that counts both classes and writes each admitted key with its position to
+// the warp's region (ranks from ballots, no atomics).  After one cluster
+// barrier every CTA reads the counts of eq. 27, takes the same route, gathers
+// the frontier keys of all CTAs through distributed shared memory and selects
+// the K-th smallest frontier key locally; each CTA then commits its own
+// entries below that key and its share of the ties, with output ranges
+// reserved by one atomic pair on the leader CTA.  Frontiers that do not fit
+// the merged list (tie runs, constant rows) and exact coarse recovery run the
+// 11+11+10 recurrence with cluster-summed histograms over the resident
+// segments, so no route re-reads HBM.
+
+// Per-CTA shared state of the cluster kernel (at offset 0 of dynamic smem).
+struct ClusterState {
+  uint64_t bar;        // mbarrier of the segment copy
+  uint32_t cnt_a;      // |{d <= T0}| in this segment
+  uint32_t cnt_b;      // |{T0 < d <= T1}| in this segment
+  uint32_t n_out;      // leader: output slots handed out
+  uint32_t n_keep;     // leader: tie slots handed out
+  int32_t timed_out;   // the segment copy did not complete in time
+  int32_t pad_[5];
+  uint32_t wcnt[16];   // class-A keys (d <= T0) found by each warp
+  uint32_t wcntb[16];  // class-B keys (T0 < d <= T1) found by each warp
+};
+static_assert(sizeof(ClusterState) % 16 == 0, "ClusterState keeps the layout 16-byte aligned");
+
+// Admitted (key, position) pairs each warp of a cluster CTA can hold (class A
+// from the front of its region, class B from the back); the merged frontier
+// of a row holds at most kMergeCap keys.  Larger frontiers (tie runs, constant
+// rows) take the histogram path over the resident segments.
+constexpr int kRegionCap = 128;
+constexpr uint32_t kMergeCap = 3 * kCoarseBins;
+
+struct ClusterLayout {
+  uint32_t state, slot, scratch, h256, hist, keys, pos, sumx, stage, total;
+};
+__host__ __device__ constexpr ClusterLayout cluster_layout() {
+  ClusterLayout l{};
+  uint32_t o = 0;
+  l.state = o;
+  o = align16(o + (uint32_t)sizeof(ClusterState));
+  l.slot = o;
+  o = align16(o + (uint32_t)sizeof(Slot));
+  l.scratch = o;
+  o = align16(o + 2 * (uint32_t)sizeof(GroupScratch));
+  l.h256 = o;  // private: region offsets and counts of the merged list
+  o = align16(o + 256u * 4u);
+  l.hist = o;  // private 2048-bin histogram of the selections
+  o = align16(o + kCoarseBins * 4u);
+  l.keys = o;  // published: per-warp regions of admitted keys (fallback: an exchange histogram)
+  o = align16(o + (kClusterThreads / 32) * kRegionCap * 4u);
+  l.pos = o;   // private: their segment positions
+  o = align16(o + (kClusterThreads / 32) * kRegionCap * 2u);
+  l.sumx = o;  // private merged frontier; or [summed histogram | published exchange histogram]
+  o = align16(o + kMergeCap * 4u);
+  o = (o + 127u) & ~127u;
+  l.stage = o;  // the resident segment
+  o += kClusterStage * 4u;
+  l.total = o;
+  return l;
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Full cluster barrier with release/acquire ordering of shared memory.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t peer_addr(uint32_t local, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(local), "r"(rank));
+  return a;
+}
+// Peer loads are volatile (they stay in order with the cluster barriers, which
+// clobber memory) but carry no memory clobber of their own, so independent
+// loads can be in flight together.
+__device__ __forceinline__ uint4 ld_peer4(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_peer(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t atom_add_peer(uint32_t a, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(a), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+// One TMA bulk copy global -> this CTA's shared memory, completing on `bar`.
+// Both addresses 16-byte aligned, bytes a positive multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0u;
+}
+// Bounded wait for phase 0 of `bar`; false when the limit ran out.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar) {
+  for (int it = 0; it < (1 << 20); ++it)
+    if (mbar_try_wait(bar, 0u)) return true;
+  return false;
+}
+
+// Sums histogram `local` (nbins, a multiple of 4, at most 4 per thread) over
+// the P CTAs of the cluster into `sum`.  Group barrier before return.
+template <class G>
+__device__ __forceinline__ void cluster_hist_sum(const uint32_t* local, uint32_t* sum, int nbins,
+                                                 int P) {
+  const int t = G::rank();
+  if (4 * t < nbins) {
+    const uint32_t la = smem_addr(local + 4 * t);
+    uint4 acc = make_uint4(0u, 0u, 0u, 0u);
+    for (int q = 0; q < P; ++q) {
+      const uint4 v = ld_peer4(peer_addr(la, (uint32_t)q));
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    *reinterpret_cast<uint4*>(sum + 4 * t) = acc;
+  }
+  G::sync();
+}
+
+// The frontier of the cluster kernel is a key interval: lo_open < d <= hi
+// (lo_open absent on the sampled routes).  Keys at or below lo_open are the
+// E0 of exact coarse recovery (committed outright).
+struct KeyBand {
+  uint32_t lo;  // exclusive lower key bound
+  uint32_t hi;  // inclusive upper key bound
+  bool has_lo;
+  __device__ __forceinline__ bool in(uint32_t d) const { return d <= hi && (!has_lo || d > lo); }
+  __device__ __forceinline__ bool below(uint32_t d) const { return has_lo && d <= lo; }
+};
+
+// Screen of four staged scores against an inclusive key bound T: false only
+// when none of them can have key <= T.  For a non-negative cutoff score the
+// key order on candidates is the signed order of the raw bits.
+struct Screen {
+  uint32_t T;
+  int C;
+  bool fast;
+  __device__ __forceinline__ explicit Screen(uint32_t T_) : T(T_) {
+    const uint32_t b = bits_from_desc(T_);
+    fast = (b & 0x80000000u) == 0u;
+    C = (int)b;
+  }
+  __device__ __forceinline__ bool any(const uint4& v) const {
+    if (fast) return max(max((int)v.x, (int)v.y), max((int)v.z, (int)v.w)) >= C;
+    return min(min(desc_key(v.x), desc_key(v.y)), min(desc_key(v.z), desc_key(v.w))) <= T;
+  }
+};
+
+
+// Block-wide exclusive scan of one packed value per thread (the two 16-bit
+// halves must not carry); returns this thread's exclusive prefix and the
+// group total in `total`.
+template <class G>
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, GroupScratch& sc,
+                                                         uint32_t& total) {
+  const int tid = G::rank(), lane = tid & 31, warp = tid >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) sc.warp_sums[warp] = incl;
+  G::sync();
+  uint32_t w = lane < G::kWarps ? sc.warp_sums[lane] : 0u;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFull, w, o);
+    if (lane >= o) w += y;
+  }
+  const uint32_t before = warp ? __shfl_sync(kFull, w, warp - 1) : 0u;
+  total = __shfl_sync(kFull, w, G::kWarps - 1);
+  G::sync();  // warp_sums may be reused on return
+  return before + incl - v;
+}
+
+// Block-wide min and max of one value per thread.
+template <class G>
+__device__ __forceinline__ void block_min_max(uint32_t vmin, uint32_t vmax, GroupScratch& sc,
+                                              uint32_t& omin, uint32_t& omax) {
+  const int tid = G::rank(), lane = tid & 31, warp = tid >> 5;
+  vmin = __reduce_min_sync(kFull, vmin);
+  vmax = __reduce_max_sync(kFull, vmax);
+  if (lane == 0) {
+    sc.warp_sums[warp] = vmin;
+    sc.warp_sums[16 + warp] = vmax;
+  }
+  G::sync();
+  uint32_t a = lane < G::kWarps ? sc.warp_sums[lane] : 0xFFFFFFFFu;
+  uint32_t b = lane < G::kWarps ? sc.warp_sums[16 + lane] : 0u;
+  omin = __reduce_min_sync(kFull, a);
+  omax = __reduce_max_sync(kFull, b);
+  G::sync();
+}
+
+// Histogram add by a whole warp: one shared atomic when every active lane has
+// the same bin (tie runs), one per lane otherwise.
+__device__ __forceinline__ void hist_add_same(uint32_t* hist, uint32_t bin, bool active) {
+  const uint32_t act = __ballot_sync(kFull, active);
+  if (act == 0u) return;
+  const int first = __ffs(act) - 1;
+  const uint32_t b0 = __shfl_sync(kFull, bin, first);
+  if (__ballot_sync(kFull, active && bin == b0) == act) {
+    if ((int)(threadIdx.x & 31) == first) atomicAdd(&hist[b0], (uint32_t)__popc(act));
+  } else if (active) {
+    atomicAdd(&hist[bin], 1u);
+  }
+}
+
+// Result of Phase 3: commit every frontier key below `commit_below`, then
+// `ties` keys equal to `tie_key`.
+struct Cut {
+  uint64_t commit_below;
+  uint32_t tie_key;
+  uint32_t ties;
+  bool bad;
+};
+
+// The t-th smallest (1 <= t <= their count) of the values in v[0, n) that
+// are <= vhi, by radix rounds of 11-bit digits taken over the values' own
+// range [min, max] (so that clustered values still spread over the bins).
+// Returns the value and, in `below`, how many considered values are smaller;
+// `bad` when no value is considered or the counts are inconsistent.
+template <class G>
+__device__ uint32_t small_select(const uint32_t* v, uint32_t n, uint32_t vhi, uint32_t t,
+                                 uint32_t* hist, GroupScratch& sc, uint32_t& below, bool& bad) {
+  const int tid = G::rank();
+  uint32_t mn = 0xFFFFFFFFu, mx = 0u;
+  for (uint32_t i = tid; i < n; i += G::kThreads) {
+    const uint32_t x = v[i];
+    if (x <= vhi) {
+      mn = min(mn, x);
+      mx = max(mx, x);
+    }
+  }
+  uint32_t kmin, kmax;
+  block_min_max<G>(mn, mx, sc, kmin, kmax);
+  below = 0u;
+  bad = kmin > kmax;
+  if (bad) return 0u;
+  uint64_t qlo = kmin, qhi = (uint64_t)kmax + 1u;
+  const uint32_t nr = (n + 31u) & ~31u;
+  while (qhi - qlo > 1u) {
+    const int s = 64 - __clzll((long long)(qhi - qlo - 1u));
+    const int width = s < 11 ? s : 11;
+    const int shift = s - width;
+    const int nbins = (1 << width) < 128 ? 128 : (1 << width);
+    clear_hist<G>(hist, nbins);
+    G::sync();
+    for (uint32_t i = tid; i < nr; i += G::kThreads) {
+      const uint32_t x = i < n ? v[i] : 0xFFFFFFFFu;
+      const bool in = i < n && x <= vhi && (uint64_t)x >= qlo && (uint64_t)x < qhi;
+      hist_add_same(hist, in ? (uint32_t)(((uint64_t)x - qlo) >> shift) : 0u, in);
+    }
+    G::sync();
+    find_boundaries<G>(hist, sc, nbins, 1, t, 0u);
+    const int b = sc.res_bin[0];
+    const uint32_t bl = sc.res_below[0];
+    if (b < 0) {
+      bad = true;
+      return 0u;
+    }
+    qlo += (uint64_t)b << shift;
+    qhi = qlo + ((uint64_t)1 << shift);
+    below += bl;
+    t -= bl;
+  }
+  return (uint32_t)qlo;
+}
+
+// Phase 3 over the cluster for rows whose frontier does not fit a merged
+// list (tie-heavy rows, exact coarse recovery): 11+11+10 digits of the key,
+// each round's histogram summed over the cluster through DSMEM.  `xa` and
+// `xc` alternate as the published buffer; `sum` is private.
+template <class G>
+__device__ Cut cluster_select(const uint4* st4, int n, const KeyBand& F, uint32_t k, uint32_t* xa,
+                              uint32_t* xc, uint32_t* sum, GroupScratch& sc, int P) {
+  const int tid = G::rank();
+  const int nv4 = (n + 3) >> 2;
+  Cut cut{0, 0u, 0u, false};
+  uint32_t prefix = 0u;
+  uint32_t* nxt = xa;
+  for (int j = 0; j < 3; ++j) {
+    const int width = j == 2 ? 10 : 11;
+    const int shift = j == 0 ? 21 : (j == 1 ? 10 : 0);
+    const int pshift = shift + width;  // digits above j
+    clear_hist<G>(nxt, kCoarseBins);
+    G::sync();
+    {
+      const uint32_t top = j == 0 ? 0xFFFFFFFFu
+                                  : (uint32_t)((((uint64_t)prefix + 1u) << pshift) - 1u);
+      const Screen scr(top < F.hi ? top : F.hi);
+      RunHist rh;
+      for (int t = tid; t < nv4; t += G::kThreads) {
+        const uint4 v = st4[t];
+        if (!scr.any(v)) continue;
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t d = desc_key(u[e]);
+          if (4 * t + e < n && F.in(d) && (j == 0 || (d >> pshift) == prefix))
+            rh.add(nxt, digit(d, j));
+        }
+      }
+      rh.flush(nxt);
+    }
+    G::sync();
+    cluster_sync_all();
+    cluster_hist_sum<G>(nxt, sum, 1 << width, P);
+    nxt = nxt == xa ? xc : xa;
+    find_boundaries<G>(sum, sc, 1 << width, 1, k, 0u);
+    const int b = sc.res_bin[0];
+    const uint32_t below = sc.res_below[0], cnt = sc.res_cnt[0];
+    if (b < 0) {
+      cut.bad = true;
+      return cut;
+    }
+    prefix = (prefix << width) | (uint32_t)b;
+    if (below + cnt == k) {
+      cut.commit_below = (uint64_t)(prefix + 1u) << shift;
+      return cut;
+    }
+    k -= below;
+    if (j == 2) {
+      cut.commit_below = prefix;
+      cut.tie_key = prefix;
+      cut.ties = k;
+    }
+  }
+  return cut;
+}
+
+// Commit of a cluster CTA: every accepted key goes to
+// [0, K - ties), the first `ties` keys equal to the tie key to [K - ties, K)
+// over the cluster.  A block scan of the per-thread counts gives every thread
+// its offsets and each CTA reserves its ranges with one atomic pair on the
+// leader's counters, so placing the entries needs no atomics.  `visit(pass,
+// fn)` calls fn(key, index) for this thread's candidate entries, in the same
+// order on both passes.
+template <class G, class Visit>
+__device__ void cluster_commit(const Visit& visit, uint64_t commit_below, uint32_t tie_key,
+                               uint32_t ties, bool bad, uint32_t n_out_addr, uint32_t n_keep_addr,
+                               GroupScratch& sc, int32_t* out_row, int K) {
+  const int tid = G::rank();
+  uint32_t nc = 0u, nt = 0u;
+  if (!bad) {
+    visit([&](uint32_t d, bool e0, int32_t) {
+      if (e0 || (uint64_t)d < commit_below)
+        ++nc;
+      else if (ties > 0u && d == tie_key)
+        ++nt;
+    });
+  }
+  uint32_t tot;
+  const uint32_t ex = block_exclusive_scan<G>(nc | (nt << 16), sc, tot);
+  if (tid == 0) {
+    const uint32_t NC = tot & 0xFFFFu, NT = tot >> 16;
+    const uint32_t bc = NC ? atom_add_peer(n_out_addr, NC) : 0u;
+    const uint32_t bt = NT ? atom_add_peer(n_keep_addr, NT) : 0u;
+    sc.res_below[0] = bc;                       // first commit slot
+    sc.res_below[1] = (uint32_t)K - ties + bt;  // first tie slot
+    sc.res_cnt[1] = bt >= ties ? 0u : min(NT, ties - bt);  // ties this CTA fills
+  }
+  G::sync();
+  if (!bad && (nc | nt) != 0u) {
+    uint32_t oc = sc.res_below[0] + (ex & 0xFFFFu);
+    uint32_t ot = ex >> 16;
+    const uint32_t tbase = sc.res_below[1], take = sc.res_cnt[1];
+    visit([&](uint32_t d, bool e0, int32_t idx) {
+      if (e0 || (uint64_t)d < commit_below) {
+        if (oc < (uint32_t)K) out_row[oc] = idx;
+        ++oc;
+      } else if (ties > 0u && d == tie_key) {
+        if (ot < take && tbase + ot < (uint32_t)K) out_row[tbase + ot] = idx;
+        ++ot;
+      }
+    });
+  }
+}
+
+__global__ void __launch_bounds__(kClusterThreads, 2) cluster_split_kernel(Params p) {
+  using G = CtaGroup<kClusterThreads>;
+  constexpr int kWarps = kClusterThreads / 32;
+  unsigned char* sm = smem_base();
+  constexpr ClusterLayout lay = cluster_layout();
+  ClusterState& cs = *reinterpret_cast<ClusterState*>(sm + lay.state);
+  Slot& sl = *reinterpret_cast<Slot*>(sm + lay.slot);
+  GroupScratch& sc = *reinterpret_cast<GroupScratch*>(sm + lay.scratch);
+  uint32_t* h256 = reinterpret_cast<uint32_t*>(sm + lay.h256);  // merged-list offsets
+  uint32_t* hist = reinterpret_cast<uint32_t*>(sm + lay.hist);  // private
+  uint32_t* keys = reinterpret_cast<uint32_t*>(sm + lay.keys);  // [kWarps][kRegionCap]
+  uint16_t* pos = reinterpret_cast<uint16_t*>(sm + lay.pos);    // [kWarps][kRegionCap]
+  uint32_t* sumx = reinterpret_cast<uint32_t*>(sm + lay.sumx);  // [kMergeCap]
+  uint32_t* stage = reinterpret_cast<uint32_t*>(sm + lay.stage);
+  uint32_t* sum = sumx;                  // summed histogram (private)
+  uint32_t* xC = sumx + kCoarseBins;     // published: view samples or a histogram
+  uint32_t* xA = keys;                   // published histogram on the fallback paths
+  const int r = blockIdx.y;
+  const uint32_t q = cluster_ctarank();
+  const int P = p.P;
+  const int K = p.K;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t lt = lanemask_lt();
+  // Every CTA of a cluster shares r, so these exits are cluster-uniform.
+  if (r >= live_rows(p)) return;
+  const float* row = p.logits + (int64_t)r * p.pitch;
+  const int L = row_length(p, r);
+  int32_t* out_row = p.out + (int64_t)r * K;
+  if (L <= K) {
+    if (q == 0) {
+      write_pad_row<G>(out_row, L, K);
+      if (tid == 0) write_trace(p, r, EXACT_TOPK_ROUTE_PAD, -1, -1, -1, -1, -1, -1, -1);
+    }
+    return;
+  }
+  int lo, hi;
+  segment_bounds(L, P, (int)q, lo, hi);
+  int n = hi - lo;  // <= kClusterStage by the plan (checked on the host)
+  if (n > kClusterStage) {
+    n = kClusterStage;  // never taken for a valid plan; the row's result is flagged
+    if (threadIdx.x == 0) flag_status(p.counters, 1);
+  }
+  const float* src = row + lo;
+  const bool bulk = (reinterpret_cast<uintptr_t>(src) & 15u) == 0u;
+  const int nb = bulk ? (n & ~3) : 0;  // scores moved by the bulk copy
+  const uint32_t bar = smem_addr(&cs.bar);
+
+  // Phase-1 view (eq. 13), replicated in every CTA of the cluster as in the
+  // KV-split of section 4.5: its loads are issued ahead of the segment copy so
+  // that they do not queue behind it.
+  const int a = view_phase(r, p.s, p.s_bits);
+  const int vsize = view_size(L, a, p.s);
+  const bool sampled = p.prev == nullptr && vsize >= (p.dual ? p.q1 : p.q0);
+  constexpr int kViewAhead = 4;  // view loads per thread issued before the copy
+  uint32_t vu[kViewAhead];
+#pragma unroll
+  for (int k = 0; k < kViewAhead; ++k) {
+    const int t = k * G::kThreads + tid;
+    vu[k] = (sampled && t < vsize)
+                ? __ldg(reinterpret_cast<const unsigned int*>(row) + a + (int64_t)t * p.s)
+                : 0u;
+  }
+
+  // ---- segment copy (TMA bulk), in flight during Phase 1 ----
+  if (tid == 0) {
+    mbar_init(bar, 1u);
+    if (nb > 0) bulk_copy_g2s(smem_addr(stage), src, (uint32_t)nb * 4u, bar);
+    cs.cnt_a = 0u;
+    cs.cnt_b = 0u;
+    cs.n_out = 0u;
+    cs.n_keep = 0u;
+    cs.timed_out = 0;
+    sl.tau0 = -1;
+    sl.tau1 = -1;
+  }
+  for (int t = nb + tid; t < n; t += G::kThreads) stage[t] = ld_stream1(src + t);
+
+  // ---- Phase 1 ----
+  // The view is split like the row.  Each CTA publishes the coarse bins of
+  // its own view positions; every CTA gathers all of them (at most kMergeCap)
+  // and selects the q0-th and q1-th smallest bins, which are tau0 and tau1 of
+  // eq. 15 (the inclusive prefix of the view histogram first reaches q at the
+  // q-th smallest bin).  Longer views are histogrammed and summed instead.
+  // The optional guess source gathers its K scores from HBM.
+  bool guess = false, direct = false;
+  if (p.prev != nullptr && guess_bin<G>(p, row, L, r, sc, sl)) {
+    guess = true;
+  } else {
+    direct = vsize < (p.dual ? p.q1 : p.q0);
+  }
+  if (!guess && !direct) {
+    clear_hist<G>(sum, kCoarseBins);
+    G::sync();
+#pragma unroll
+    for (int k = 0; k < kViewAhead; ++k) {
+      const int t = k * G::kThreads + tid;
+      if (t < vsize) {
+        const uint32_t u =
+            sampled ? vu[k] : __ldg(reinterpret_cast<const unsigned int*>(row) + a + (int64_t)t * p.s);
+        atomicAdd(&sum[coarse_bin(u)], 1u);
+      }
+    }
+    for (int t = kViewAhead * G::kThreads + tid; t < vsize; t += G::kThreads)
+      atomicAdd(&sum[coarse_bin(__ldg(reinterpret_cast<const unsigned int*>(row) + a +
+                                      (int64_t)t * p.s))],
+                1u);
+    G::sync();
+    view_cutoffs<G>(p, sum, sc, sl);
+  }
+  uint32_t T0 = sl.T0, T1 = sl.T1;
+  if (guess || !(p.dual && T1 > T0)) T1 = T0;
+  const int tau0 = sl.tau0, tau1 = guess ? -1 : sl.tau1;
+  // One thread polls the copy's barrier; the rest wait at the CTA barrier.
+  if (tid == 0 && nb > 0 && !mbar_wait_bounded(bar)) cs.timed_out = 1;
+  G::sync();
+  const uint4* st4 = reinterpret_cast<const uint4*>(stage);
+  const int nv4 = (n + 3) >> 2;
+
+  // ---- Phase 2 over the resident segment (one pass) ----
+  // Both classes are counted per thread; every admitted key (d <= T1) and its
+  // position go to the warp's region at a rank taken from a ballot, so the
+  // pass needs no atomics.
+  if (!direct) {
+    uint32_t wa = 0u, wb = 0u;  // warp-uniform: class A / class B keys this warp found
+    uint32_t* wk = keys + warp * kRegionCap;
+    uint16_t* wp = pos + warp * kRegionCap;
+    const int nv4r = (nv4 + 31) & ~31;
+    for (int t = tid; t < nv4r; t += G::kThreads) {
+      uint4 v = make_uint4(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu);
+      if (t < nv4) v = st4[t];
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t d = desc_key(u[e]);
+        const bool in = t < nv4 && 4 * t + e < n;
+        const bool isa = in && d <= T0;
+        const bool isb = in && !isa && d <= T1;
+        const uint32_t ba = __ballot_sync(kFull, isa);
+        const uint32_t bb = __ballot_sync(kFull, isb);
+        if ((ba | bb) != 0u) {
+          const uint32_t ra = wa + (uint32_t)__popc(ba & lt);
+          const uint32_t rb = wb + (uint32_t)__popc(bb & lt);
+          if (isa && ra + wb < (uint32_t)kRegionCap) {
+            wk[ra] = d;
+            wp[ra] = (uint16_t)(4 * t + e);
+          } else if (isb && wa + rb < (uint32_t)kRegionCap) {
+            wk[kRegionCap - 1 - rb] = d;
+            wp[kRegionCap - 1 - rb] = (uint16_t)(4 * t + e);
+          }
+          wa += (uint32_t)__popc(ba);
+          wb += (uint32_t)__popc(bb);
+        }
+      }
+    }
+    if (lane == 0) {
+      cs.wcnt[warp] = wa;
+      cs.wcntb[warp] = wb;
+      atomicAdd(&cs.cnt_a, wa);
+      atomicAdd(&cs.cnt_b, wb);
+    }
+  } else if (lane == 0) {
+    cs.wcnt[warp] = 0u;
+    cs.wcntb[warp] = 0u;
+  }
+  G::sync();
+  cluster_sync_all();  // step 0: counts and key regions published
+
+  // Certification over the cluster (eq. 27) and the layout of the merged
+  // frontier: sub-list 2 (16 j + w) + c is class c of warp w's region in CTA
+  // j; h256[r] is its offset (class B only on the band route).  One warp
+  // issues every peer load at once.
+  if (warp == 0) {
+    uint32_t ca = 0u, cb = 0u;
+    if (lane < P) {
+      ca = ld_peer(peer_addr(smem_addr(&cs.cnt_a), (uint32_t)lane));
+      cb = ld_peer(peer_addr(smem_addr(&cs.cnt_b), (uint32_t)lane));
+    }
+    uint32_t c[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int rr = 8 * lane + i, j = rr >> 5, w = (rr >> 1) & 15, cls = rr & 1;
+      c[i] = 0u;
+      if (j < P)
+        c[i] = ld_peer(peer_addr(smem_addr(cls ? &cs.wcntb[w] : &cs.wcnt[w]), (uint32_t)j));
+    }
+    ca = __reduce_add_sync(kFull, ca);
+    cb = __reduce_add_sync(kFull, cb);
+    const bool band = !guess && p.dual && ca < (uint32_t)K;
+    bool over = false;
+    uint32_t s8 = 0u;
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+      over = over || c[i] + c[i + 1] > (uint32_t)kRegionCap;
+      if (!band) c[i + 1] = 0u;
+      s8 += c[i] + c[i + 1];
+    }
+    uint32_t incl = s8;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += y;
+    }
+    uint32_t run = incl - s8;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      h256[8 * lane + i] = run;
+      run += c[i];
+    }
+    over = __any_sync(kFull, over);
+    if (lane == 0) {
+      sl.c0 = (int)ca;
+      sl.c1 = (int)cb;
+      sc.bcast = over ? 1 : 0;
+    }
+  }
+  G::sync();
+  const uint32_t C0 = (uint32_t)sl.c0, CB = (uint32_t)sl.c1;
+  int route;
+  bool recover;
+  if (direct) {
+    route = EXACT_TOPK_ROUTE_DIRECT_EXACT;
+    recover = true;
+  } else if (guess) {
+    recover = C0 < (uint32_t)K;
+    route = recover ? EXACT_TOPK_ROUTE_GUESS_EXACT : EXACT_TOPK_ROUTE_GUESS;
+  } else if (C0 >= (uint32_t)K) {
+    route = EXACT_TOPK_ROUTE_PRIMARY;
+    recover = false;
+  } else if (p.dual) {
+    recover = C0 + CB < (uint32_t)K;
+    route = recover ? EXACT_TOPK_ROUTE_EXACT_AFTER_BAND : EXACT_TOPK_ROUTE_BAND;
+  } else {
+    route = EXACT_TOPK_ROUTE_EXACT_NO_BAND;
+    recover = true;
+  }
+  const bool band_tried = !direct && !guess && p.dual && C0 < (uint32_t)K;
+  const int c0_trace = direct ? -1 : (int)C0;
+  const int c1_trace = band_tried ? (int)(C0 + CB) : -1;
+
+  KeyBand F;
+  uint32_t k = (uint32_t)K;
+  int tstar = -1, e0 = 0, q0n = 0;
+  Cut cut{0, 0u, 0u, false};
+  const bool with_band = route == EXACT_TOPK_ROUTE_BAND;
+  const uint32_t nfront = with_band ? C0 + CB : C0;
+  const bool list_path = !recover && sc.bcast == 0 && nfront <= kMergeCap;
+  if (!recover) {
+    const bool with_b = route == EXACT_TOPK_ROUTE_BAND;
+    F.has_lo = false;
+    F.lo = 0u;
+    F.hi = with_b ? T1 : T0;
+    q0n = with_b ? (int)(C0 + CB) : (int)C0;
+  }
+  if (list_path) {
+    // Merge every CTA's regions (independent DSMEM loads), then select the
+    // K-th smallest frontier key locally: commit the keys below it and fill
+    // the rest from its ties (eqs. 22-25 reach the same threshold).
+    const uint32_t total = nfront;
+    // Warp w copies sub-lists w, w + 16, ...: consecutive keys of one peer
+    // region per request, all requests of a warp in flight together.
+    const int nsub = 2 * P * kWarps;
+    const uint32_t kb = smem_addr(keys);
+    for (int r0 = warp; r0 < nsub; r0 += 4 * kWarps) {
+      uint32_t vv[4][4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int rr = r0 + b * kWarps;
+#pragma unroll
+        for (int x = 0; x < 4; ++x) vv[b][x] = 0u;
+        if (rr < nsub) {
+          const uint32_t beg = h256[rr], end = rr + 1 < nsub ? h256[rr + 1] : total;
+          const uint32_t j = (uint32_t)(rr >> 5), w = (uint32_t)((rr >> 1) & 15);
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            const uint32_t e = (uint32_t)lane + 32u * x;
+            if (beg + e < end) {
+              const uint32_t word = w * kRegionCap + ((rr & 1) ? (uint32_t)kRegionCap - 1u - e : e);
+              vv[b][x] = ld_peer(peer_addr(kb + 4u * word, j));
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int rr = r0 + b * kWarps;
+        if (rr < nsub) {
+          const uint32_t beg = h256[rr], end = rr + 1 < nsub ? h256[rr + 1] : total;
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            const uint32_t e = (uint32_t)lane + 32u * x;
+            if (beg + e < end) sumx[beg + e] = vv[b][x];
+          }
+        }
+      }
+    }
+    G::sync();
+    uint32_t below;
+    bool bad = false;
+    const uint32_t vstar = small_select<G>(sumx, total, F.hi, k, hist, sc, below, bad);
+    cut.bad = bad;
+    cut.commit_below = vstar;
+    cut.tie_key = vstar;
+    cut.ties = k - below;
+  } else if (!recover) {
+    cut = cluster_select<G>(st4, n, F, k, xA, xC, sum, sc, P);
+  } else {
+    // Exact coarse recovery (eq. 20) over the resident row: coarse histogram,
+    // tau* = min{b : C(b) >= K}, E0 = {c < tau*}, Q0 = {c == tau*}.
+    clear_hist<G>(xA, kCoarseBins);
+    G::sync();
+    {
+      RunHist rh;
+      for (int t = tid; t < nv4; t += G::kThreads) {
+        const uint4 v = st4[t];
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (4 * t + e < n) rh.add(xA, (uint32_t)coarse_bin(u[e]));
+      }
+      rh.flush(xA);
+    }
+    G::sync();
+    cluster_sync_all();
+    cluster_hist_sum<G>(xA, sum, kCoarseBins, P);
+    find_boundaries<G>(sum, sc, kCoarseBins, 1, (uint32_t)K, 0u);
+    tstar = sc.res_bin[0];
+    e0 = (int)sc.res_below[0];
+    q0n = (int)sc.res_cnt[0];
+    exact_cutoffs<G>(sl, tstar < 0 ? 0 : tstar);
+    F.has_lo = tstar > 0;
+    F.lo = sl.T0;
+    F.hi = sl.T1;
+    k = (uint32_t)(K - e0);
+    if (tstar < 0)
+      cut.bad = true;
+    else
+      cut = cluster_select<G>(st4, n, F, k, xC, xA, sum, sc, P);
+  }
+  G::sync();  // every thread holds the cut before the commit reuses the scratch
+
+  // ---- commit ----
+  const uint32_t a_out = peer_addr(smem_addr(&cs.n_out), 0u);
+  const uint32_t a_keep = peer_addr(smem_addr(&cs.n_keep), 0u);
+  if (list_path) {
+    // candidates: this CTA's own admitted entries (regions), frontier keys only
+    // candidates: each warp visits its own region (this CTA's admitted
+    // entries), frontier keys only
+    const uint32_t ca = cs.wcnt[warp];
+    const uint32_t cb = with_band ? cs.wcntb[warp] : 0u;  // ca + cb <= kRegionCap here
+    const uint32_t* wk = keys + warp * kRegionCap;
+    const uint16_t* wp = pos + warp * kRegionCap;
+    auto visit = [&](auto&& fn) {
+      for (uint32_t i = lane; i < ca + cb; i += 32) {
+        const uint32_t x = i < ca ? i : (uint32_t)kRegionCap - 1u - (i - ca);
+        fn(wk[x], false, lo + (int32_t)wp[x]);
+      }
+    };
+    cluster_commit<G>(visit, cut.commit_below, cut.tie_key, cut.ties, cut.bad, a_out, a_keep, sc,
+                      out_row, K);
+  } else {
+    const KeyBand FF = F;
+    auto visit = [&](auto&& fn) {
+      for (int t = tid; t < nv4; t += G::kThreads) {
+        const uint4 v = st4[t];
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t d = desc_key(u[e]);
+          if (4 * t + e < n && (FF.below(d) || FF.in(d))) fn(d, FF.below(d), lo + 4 * t + e);
+        }
+      }
+    };
+    cluster_commit<G>(visit, cut.commit_below, cut.tie_key, cut.ties, cut.bad, a_out, a_keep, sc,
+                      out_row, K);
+  }
+  G::sync();
+  cluster_sync_all();  // every slot written; no CTA reads a peer after this
+
+  if (q == 0) {
+    const bool fill_ok = cs.n_out == (uint32_t)K - cut.ties && cs.n_keep >= cut.ties;
+    if (cut.bad || !fill_ok) {
+      for (int t = tid; t < K; t += G::kThreads) out_row[t] = -1;
+      if (tid == 0) flag_status(p.counters, 1);
+    }
+    if (tid == 0)
+      write_trace(p, r, route, direct ? -1 : tau0, direct ? -1 : tau1, c0_trace, c1_trace, tstar,
+                  e0, q0n);
+  }
+  if (tid == 0 && cs.timed_out) flag_status(p.counters, 4);
+}
+
 // Kernel attributes are set once per (device, kernel); later launches, which
 // may be inside a stream capture, only launch.
 constexpr int kMaxDevices = 64;
-volatile int g_attr_smem[kMaxDevices][4];
+volatile int g_attr_smem[kMaxDevices][5];
 
 template <class KernelT>
 int set_attrs(KernelT kernel, int family, size_t smem) {
@@ -1619,7 +2472,10 @@ int set_attrs(KernelT kernel, int family, size_t smem) {
 
 }  // namespace
 
-size_t shared_bytes(int family, int cap) { return smem_layout(family, cap).total; }
+size_t shared_bytes(int family, int cap) {
+  if (family == EXACT_TOPK_FAMILY_CLUSTER_SPLIT) return cluster_layout().total;
+  return smem_layout(family, cap).total;
+}
 
 int kernel_occupancy(int family, int device, int* ctas_per_sm) {
   int prev = 0;
@@ -1638,6 +2494,12 @@ int kernel_occupancy(int family, int device, int* ctas_per_sm) {
     rc = set_attrs(kv_split_kernel, EXACT_TOPK_FAMILY_KV_SPLIT, smem);
     if (rc == EXACT_TOPK_OK)
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kv_split_kernel, kKvSplitThreads, smem);
+  } else if (family == EXACT_TOPK_FAMILY_CLUSTER_SPLIT) {
+    const size_t smem = shared_bytes(family, kClusterStage);
+    rc = set_attrs(cluster_split_kernel, EXACT_TOPK_FAMILY_CLUSTER_SPLIT, smem);
+    if (rc == EXACT_TOPK_OK)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, cluster_split_kernel, kClusterThreads,
+                                                        smem);
   } else {
     const size_t smem = shared_bytes(family, kRowLocalCap);
     rc = set_attrs(row_local_exact_kernel, EXACT_TOPK_FAMILY_ROW_LOCAL_EXACT, smem);
@@ -1702,6 +2564,28 @@ int launch(const exact_topk_plan& plan, const LaunchArgs& a, cudaStream_t stream
       if (rc != EXACT_TOPK_OK) return rc;
       row_local_exact_kernel<<<plan.workers, kRowLocalThreads, smem, stream>>>(p);
       break;
+    case EXACT_TOPK_FAMILY_CLUSTER_SPLIT: {
+      if (plan.splits < 1 || plan.splits > kClusterMaxSplits ||
+          (int64_t)plan.splits * kClusterStage < plan.max_kv_len)
+        return EXACT_TOPK_ERR_BAD_PLAN;
+      rc = set_attrs(cluster_split_kernel, EXACT_TOPK_FAMILY_CLUSTER_SPLIT, smem);
+      if (rc != EXACT_TOPK_OK) return rc;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)plan.splits, (unsigned)plan.num_rows, 1u);
+      cfg.blockDim = dim3(kClusterThreads, 1u, 1u);
+      cfg.dynamicSmemBytes = smem;
+      cfg.stream = stream;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = (unsigned)plan.splits;
+      attr[0].val.clusterDim.y = 1u;
+      attr[0].val.clusterDim.z = 1u;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaLaunchKernelEx(&cfg, cluster_split_kernel, p) != cudaSuccess)
+        return EXACT_TOPK_ERR_CUDA;
+      break;
+    }
     default:
       return EXACT_TOPK_ERR_BAD_PLAN;
   }

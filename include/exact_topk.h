@@ -78,7 +78,12 @@ typedef enum exact_topk_family {
   EXACT_TOPK_FAMILY_KV_SPLIT = 2,
   /* One wide CTA per row takes the exact coarse route directly; short rows stay
      in registers (section 5.5, "Row-local exact"). */
-  EXACT_TOPK_FAMILY_ROW_LOCAL_EXACT = 3
+  EXACT_TOPK_FAMILY_ROW_LOCAL_EXACT = 3,
+  /* The P CTAs of one thread-block cluster hold one row in shared memory (at
+     most 16384 scores per CTA, P <= 8); the merge of eq. 27 and every later
+     pass run on chip through distributed shared memory (the KV-split
+     decomposition of section 4.5 for rows that fit a cluster). */
+  EXACT_TOPK_FAMILY_CLUSTER_SPLIT = 4
 } exact_topk_family;
 
 /* Route codes written to the optional per-row trace (Table 2 of section 4.6,
@@ -107,6 +112,7 @@ typedef struct exact_topk_device_info {
   int32_t persistent_ctas_per_sm; /* resident CTAs/SM of the persistent sampled kernel */
   int32_t kvsplit_ctas_per_sm;    /* resident CTAs/SM of the KV-split kernel */
   int32_t rowlocal_ctas_per_sm;   /* resident CTAs/SM of the row-local exact kernel */
+  int32_t cluster_ctas_per_sm;    /* resident CTAs/SM of the cluster split kernel */
 } exact_topk_device_info;
 
 /* Optional planner overrides: 0 (or -1 where noted) keeps the planner's choice. */
@@ -114,7 +120,8 @@ typedef struct exact_topk_plan_request {
   int32_t family;        /* exact_topk_family */
   int32_t stride;        /* view stride s: power of two in [2, 4096] */
   int32_t dual;          /* -1 planner, 0 primary-only, 1 primary + secondary boundary */
-  int32_t splits;        /* KV-split segment count P in [1, 128] */
+  int32_t splits;        /* segment count P: KV-split [1, 128]; cluster split [1, 8]
+                            with P * 16384 >= max_kv_len */
   int32_t workers;       /* persistent / row-local grid size */
   int32_t rho0_num, rho0_den; /* primary retention margin rho (K~ = rho K), default 3/2 */
   int32_t rho1_num, rho1_den; /* secondary margin rho1, default 7/4 */

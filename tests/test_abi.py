@@ -12,7 +12,7 @@ import pytest
 import exact_top_selection_gb300 as etk
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-GB300 = etk.DeviceInfo(152, 3, 3, 1)
+GB300 = etk.DeviceInfo(152, 3, 3, 1, 2)
 
 
 def declared_functions():
@@ -42,7 +42,10 @@ def test_version_and_error_strings():
 
 @pytest.mark.parametrize("M,N,K,family,stride,dual", [
     (4, 8192, 256, etk.FAMILY_ROW_LOCAL_EXACT, 64, 0),
-    (64, 65536, 2048, etk.FAMILY_KV_SPLIT, 128, 1),
+    (64, 65536, 2048, etk.FAMILY_CLUSTER_SPLIT, 128, 1),
+    (64, 131072, 2048, etk.FAMILY_CLUSTER_SPLIT, 128, 1),
+    (151, 131072, 2048, etk.FAMILY_KV_SPLIT, 128, 1),
+    (8, 140000, 2048, etk.FAMILY_KV_SPLIT, 128, 1),
     (4096, 131072, 2048, etk.FAMILY_PERSISTENT_SAMPLED, 128, 1),
     (8, 524288, 2048, etk.FAMILY_KV_SPLIT, 128, 1),
     (256, 131072, 2048, etk.FAMILY_PERSISTENT_SAMPLED, 128, 1),
@@ -57,6 +60,10 @@ def test_planner_families(M, N, K, family, stride, dual):
     if family == etk.FAMILY_KV_SPLIT:
         assert p.workers == M * p.splits and 1 <= p.splits <= 64
         assert p.workspace_bytes >= M * N * 8 + M * p.splits * 8
+    elif family == etk.FAMILY_CLUSTER_SPLIT:
+        # the fewest 16384-score segments that hold a row; no workspace
+        assert p.splits == -(-N // 16384) and p.workers == M * p.splits
+        assert p.workspace_bytes == 0 and p.cand_capacity == 16384
     elif N > p.cand_capacity:
         assert p.workers == min(M, 152 * (3 if family == 1 else 1))
         assert p.workspace_bytes >= p.workers * N * 8
@@ -80,7 +87,8 @@ def test_planner_overrides_and_errors():
             etk.make_plan(4, 100, k, device_info=GB300)
         assert e.value.code == -3
     for kw in (dict(stride=3), dict(stride=8192), dict(family=9), dict(splits=300,
-               family=etk.FAMILY_KV_SPLIT), dict(dual=2)):
+               family=etk.FAMILY_KV_SPLIT), dict(dual=2), dict(family=etk.FAMILY_CLUSTER_SPLIT,
+               splits=6), dict(family=etk.FAMILY_CLUSTER_SPLIT, splits=9)):
         with pytest.raises(etk.ExactTopKError) as e:
             etk.make_plan(4, 100000, 16, device_info=GB300, **kw)
         assert e.value.code == -7
@@ -94,7 +102,7 @@ def test_run_validates_arguments_without_touching_the_gpu():
     # Fake, never-dereferenced addresses: every call below must be rejected on
     # the host before any CUDA call.
     lib = etk.library()
-    p = etk.make_plan(64, 65536, 2048, device_info=GB300)
+    p = etk.make_plan(64, 65536, 2048, device_info=GB300, family=etk.FAMILY_KV_SPLIT)
     X, ke, out, ctr, ws = (_fake(0x100000 * i) for i in range(1, 6))
     cb, wb = p.counter_bytes, p.workspace_bytes
     run = lambda *a: lib.exact_topk_run(ctypes.byref(p), *a)

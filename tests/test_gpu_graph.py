@@ -18,6 +18,7 @@ pytestmark = pytest.mark.gpu
 
 @pytest.mark.parametrize("family,N,K", [(etk.FAMILY_PERSISTENT_SAMPLED, 70000, 2048),
                                         (etk.FAMILY_KV_SPLIT, 140000, 2048),
+                                        (etk.FAMILY_CLUSTER_SPLIT, 70000, 2048),
                                         (etk.FAMILY_ROW_LOCAL_EXACT, 8192, 256),
                                         (etk.FAMILY_ROW_LOCAL_EXACT, 20000, 512)])
 def test_capture_and_replay(family, N, K):

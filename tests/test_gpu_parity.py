@@ -19,7 +19,9 @@ from gpu_helpers import (CANARY, assert_counters_zero, compare_rows, compare_tra
 
 pytestmark = pytest.mark.gpu
 
-FAMILIES = [etk.FAMILY_PERSISTENT_SAMPLED, etk.FAMILY_KV_SPLIT, etk.FAMILY_ROW_LOCAL_EXACT]
+FAMILIES = [etk.FAMILY_PERSISTENT_SAMPLED, etk.FAMILY_KV_SPLIT, etk.FAMILY_ROW_LOCAL_EXACT,
+            etk.FAMILY_CLUSTER_SPLIT]
+SAMPLED_FAMILIES = [etk.FAMILY_PERSISTENT_SAMPLED, etk.FAMILY_KV_SPLIT, etk.FAMILY_CLUSTER_SPLIT]
 
 
 def _rows(M, N, seed, dist):
@@ -81,7 +83,7 @@ def test_scaled_workloads(name, family):
     compare_trace(tr, tr_ref)
 
 
-@pytest.mark.parametrize("family", [etk.FAMILY_PERSISTENT_SAMPLED, etk.FAMILY_KV_SPLIT])
+@pytest.mark.parametrize("family", SAMPLED_FAMILIES)
 @pytest.mark.parametrize("dual", [0, 1])
 def test_forced_routes(family, dual):
     # Table 2's routes, forced by planting large values on or off the sampled
@@ -116,7 +118,7 @@ def test_forced_routes(family, dual):
         assert tr[:3, 0].tolist() == [1, 4, 4]
 
 
-@pytest.mark.parametrize("family", [etk.FAMILY_PERSISTENT_SAMPLED, etk.FAMILY_KV_SPLIT])
+@pytest.mark.parametrize("family", SAMPLED_FAMILIES)
 def test_guess_source(family):
     M, N, K = 12, 20000, 512
     X = _rows(M, N, 5, "normal")
@@ -178,6 +180,40 @@ def test_kv_split_counts(splits):
     X, ke = Xt.numpy(), ket.numpy()
     out, tr, plan, ctr = run_gpu(X, ke, K, family=etk.FAMILY_KV_SPLIT, splits=splits)
     assert plan.splits == splits
+    compare_rows(X, ke, K, out)
+    assert_counters_zero(ctr)
+    _, tr_ref = oracle_trace_for_plan(X, ke, K, plan)
+    compare_trace(tr, tr_ref)
+
+
+@pytest.mark.parametrize("splits", [5, 6, 8])
+def test_cluster_split_counts(splits):
+    # Cluster sizes from the fewest segments that hold a row up to the
+    # portable limit; short rows leave trailing CTAs with empty segments.
+    M, N, K = 10, 70000, 2048
+    Xt, ket, K = workloads.generate("decode_batch", M=M, N=N, K=K)
+    X, ke = Xt.numpy(), ket.numpy()
+    # lengths raised past the generated ones would expose the NaN padding
+    X = np.where(np.isnan(X), np.float32(0.0), X)
+    ke[:4] = [2049, 3000, 16400, N]
+    out, tr, plan, ctr = run_gpu(X, ke, K, family=etk.FAMILY_CLUSTER_SPLIT, splits=splits)
+    assert plan.splits == splits
+    compare_rows(X, ke, K, out)
+    assert_counters_zero(ctr)
+    _, tr_ref = oracle_trace_for_plan(X, ke, K, plan)
+    compare_trace(tr, tr_ref)
+
+
+def test_cluster_split_widest_rows():
+    # Eight resident segments of 16384 scores each: the widest row a cluster
+    # holds, with ragged lengths down to a single segment.
+    M, N, K = 12, 131072, 2048
+    Xt, ket, K = workloads.generate("decode_batch", M=M, N=N, K=K)
+    X, ke = Xt.numpy(), ket.numpy()
+    X = np.where(np.isnan(X), np.float32(0.0), X)
+    ke[:6] = [N, N - 1, 16384, 16385, 114689, 40000]
+    out, tr, plan, ctr = run_gpu(X, ke, K, family=etk.FAMILY_CLUSTER_SPLIT)
+    assert plan.splits == 8
     compare_rows(X, ke, K, out)
     assert_counters_zero(ctr)
     _, tr_ref = oracle_trace_for_plan(X, ke, K, plan)
