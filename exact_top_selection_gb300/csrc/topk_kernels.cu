@@ -239,7 +239,7 @@ struct GroupScratch {
   int32_t gmax;      // guess source: worst coarse bin
   int32_t ginvalid;  // guess source: an entry outside [0, L)
   int32_t bcast;     // broadcast word
-  int32_t pad_;
+  int32_t bcast2;    // second broadcast word
 };
 
 // One row in flight: its proposal, counters and route record.
@@ -1205,22 +1205,26 @@ __device__ void exit_protocol(int32_t* counters) {
 // Phase 1, the complete-row pass with its certification (band rescue, exact
 // coarse recovery), and Phase 3.  Rows after the first wave are claimed from a
 // device counter in completion order.
-// Claims the next row and starts copying its view (Phase 1 input) into
-// shared memory, so that the copies overlap this row's refinement.
+// Claims the next row (in completion order: load balance across the grid)
+// and starts copying its view (Phase 1 input) into shared memory, so that the
+// copies overlap this row's refinement.
 __device__ int claim_and_prefetch(const Params& p, int M, Slot& sl, GroupScratch& sc,
                                   uint32_t* view) {
-  if (threadIdx.x == 0) sc.bcast = (int)gridDim.x + atomicAdd(p.counters + kCtrQueue, 1);
+  if (threadIdx.x == 0) {
+    const int nr = (int)gridDim.x + atomicAdd(p.counters + kCtrQueue, 1);
+    sc.bcast = nr;
+    sc.bcast2 = nr < M ? row_length(p, nr) : 0;
+  }
   __syncthreads();
   const int nr = sc.bcast;
   int npre = 0;
   if (nr < M && p.prev == nullptr) {
-    const int L = row_length(p, nr);
+    const int L = sc.bcast2;
     const int a = view_phase(nr, p.s, p.s_bits);
     const int nv = view_size(L, a, p.s);
     const int qmax = p.dual ? p.q1 : p.q0;
     if (L > p.K && nv >= qmax) {
       npre = nv < kViewPrefetch ? nv : kViewPrefetch;
-      npre -= npre % kPersistentThreads;  // whole rounds of the thread layout
       const float* row = p.logits + (int64_t)nr * p.pitch;
       for (int t = threadIdx.x; t < npre; t += kPersistentThreads)
         cp_async4(view + t, row + a + (int64_t)t * p.s);
@@ -1661,14 +1665,13 @@ struct ClusterState {
   uint32_t n_keep;     // leader: tie slots handed out
   int32_t timed_out;   // the segment copy did not complete in time
   int32_t pad_[5];
-  uint32_t wcnt[16];   // class-A keys (d <= T0) found by each warp
-  uint32_t wcntb[16];  // class-B keys (T0 < d <= T1) found by each warp
+  uint32_t wcnt[16];   // admitted keys (d <= T1) found by each warp
+  uint32_t pad2_[16];
 };
 static_assert(sizeof(ClusterState) % 16 == 0, "ClusterState keeps the layout 16-byte aligned");
 
-// Admitted (key, position) pairs each warp of a cluster CTA can hold (class A
-// from the front of its region, class B from the back); the merged frontier
-// of a row holds at most kMergeCap keys.  Larger frontiers (tie runs, constant
+// Admitted (key, position) pairs each warp of a cluster CTA can hold; the
+// merged list of a row holds at most kMergeCap keys.  Larger frontiers (tie runs, constant
 // rows) take the histogram path over the resident segments.
 constexpr int kRegionCap = 128;
 constexpr uint32_t kMergeCap = 3 * kCoarseBins;
@@ -1935,7 +1938,7 @@ __device__ uint32_t small_select(const uint32_t* v, uint32_t n, uint32_t vhi, ui
     G::sync();
     find_boundaries<G>(hist, sc, nbins, 1, t, 0u);
     const int b = sc.res_bin[0];
-    const uint32_t bl = sc.res_below[0];
+    const uint32_t bl = sc.res_below[0], cnt = sc.res_cnt[0];
     if (b < 0) {
       bad = true;
       return 0u;
@@ -1944,6 +1947,51 @@ __device__ uint32_t small_select(const uint32_t* v, uint32_t n, uint32_t vhi, ui
     qhi = qlo + ((uint64_t)1 << shift);
     below += bl;
     t -= bl;
+    if (cnt <= 32u && qhi - qlo > 1u) {
+      // At most 32 values left in the bucket: one warp ranks them directly
+      // instead of further radix rounds.
+      G::sync();  // every thread has read the finder's results
+      if (tid == 0) sc.bcast = 0;
+      G::sync();
+      uint32_t* buf = hist;  // free after the finder
+      for (uint32_t i = tid; i < n; i += G::kThreads) {
+        const uint32_t x = v[i];
+        if (x <= vhi && (uint64_t)x >= qlo && (uint64_t)x < qhi) {
+          const int slot = atomicAdd(&sc.bcast, 1);
+          if (slot < 32) buf[slot] = x;
+        }
+      }
+      G::sync();
+      if (tid < 32) {
+        const int m = min(sc.bcast, 32);
+        const bool valid = tid < m;
+        const uint32_t x = valid ? buf[tid] : 0u;
+        uint32_t less = 0u, eq = 0u;
+        for (int j = 0; j < 32; ++j) {
+          const uint32_t y = __shfl_sync(kFull, x, j);
+          if (j < m) {
+            less += y < x ? 1u : 0u;
+            eq += y == x ? 1u : 0u;
+          }
+        }
+        const uint32_t hit = __ballot_sync(kFull, valid && less < t && t <= less + eq);
+        const int src = hit ? __ffs(hit) - 1 : 0;
+        const uint32_t vx = __shfl_sync(kFull, x, src);
+        const uint32_t vl = __shfl_sync(kFull, less, src);
+        if (tid == 0) {
+          sc.res_bin[1] = hit ? 1 : -1;
+          sc.res_cnt[1] = vx;
+          sc.res_below[1] = vl;
+        }
+      }
+      G::sync();
+      if (sc.res_bin[1] < 0) {
+        bad = true;
+        return 0u;
+      }
+      below += sc.res_below[1];
+      return sc.res_cnt[1];
+    }
   }
   return (uint32_t)qlo;
 }
@@ -2060,7 +2108,7 @@ __device__ void cluster_commit(const Visit& visit, uint64_t commit_below, uint32
 
 __global__ void __launch_bounds__(kClusterThreads, 2) cluster_split_kernel(Params p) {
   using G = CtaGroup<kClusterThreads>;
-  constexpr int kWarps = kClusterThreads / 32;
+  static_assert(kClusterThreads / 32 == 16, "the merged-list table assumes 16 warps per CTA");
   unsigned char* sm = smem_base();
   constexpr ClusterLayout lay = cluster_layout();
   ClusterState& cs = *reinterpret_cast<ClusterState*>(sm + lay.state);
@@ -2181,7 +2229,10 @@ __global__ void __launch_bounds__(kClusterThreads, 2) cluster_split_kernel(Param
   // position go to the warp's region at a rank taken from a ballot, so the
   // pass needs no atomics.
   if (!direct) {
-    uint32_t wa = 0u, wb = 0u;  // warp-uniform: class A / class B keys this warp found
+    // one ballot per score: every admitted key (d <= T1) and its position go
+    // to the warp's region; its class (A: d <= T0) follows from the key.
+    uint32_t wc = 0u;   // warp-uniform: admitted keys this warp found
+    uint32_t ca = 0u;   // this lane's class-A keys
     uint32_t* wk = keys + warp * kRegionCap;
     uint16_t* wp = pos + warp * kRegionCap;
     const int nv4r = (nv4 + 31) & ~31;
@@ -2192,78 +2243,65 @@ __global__ void __launch_bounds__(kClusterThreads, 2) cluster_split_kernel(Param
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const uint32_t d = desc_key(u[e]);
-        const bool in = t < nv4 && 4 * t + e < n;
-        const bool isa = in && d <= T0;
-        const bool isb = in && !isa && d <= T1;
-        const uint32_t ba = __ballot_sync(kFull, isa);
-        const uint32_t bb = __ballot_sync(kFull, isb);
-        if ((ba | bb) != 0u) {
-          const uint32_t ra = wa + (uint32_t)__popc(ba & lt);
-          const uint32_t rb = wb + (uint32_t)__popc(bb & lt);
-          if (isa && ra + wb < (uint32_t)kRegionCap) {
-            wk[ra] = d;
-            wp[ra] = (uint16_t)(4 * t + e);
-          } else if (isb && wa + rb < (uint32_t)kRegionCap) {
-            wk[kRegionCap - 1 - rb] = d;
-            wp[kRegionCap - 1 - rb] = (uint16_t)(4 * t + e);
+        const bool adm = t < nv4 && 4 * t + e < n && d <= T1;
+        ca += (adm && d <= T0) ? 1u : 0u;
+        const uint32_t bal = __ballot_sync(kFull, adm);
+        if (bal != 0u) {
+          const uint32_t rk = wc + (uint32_t)__popc(bal & lt);
+          if (adm && rk < (uint32_t)kRegionCap) {
+            wk[rk] = d;
+            wp[rk] = (uint16_t)(4 * t + e);
           }
-          wa += (uint32_t)__popc(ba);
-          wb += (uint32_t)__popc(bb);
+          wc += (uint32_t)__popc(bal);
         }
       }
     }
+    ca = __reduce_add_sync(kFull, ca);
     if (lane == 0) {
-      cs.wcnt[warp] = wa;
-      cs.wcntb[warp] = wb;
-      atomicAdd(&cs.cnt_a, wa);
-      atomicAdd(&cs.cnt_b, wb);
+      cs.wcnt[warp] = wc;
+      atomicAdd(&cs.cnt_a, ca);
+      atomicAdd(&cs.cnt_b, wc - ca);
     }
   } else if (lane == 0) {
     cs.wcnt[warp] = 0u;
-    cs.wcntb[warp] = 0u;
   }
   G::sync();
   cluster_sync_all();  // step 0: counts and key regions published
 
   // Certification over the cluster (eq. 27) and the layout of the merged
-  // frontier: sub-list 2 (16 j + w) + c is class c of warp w's region in CTA
-  // j; h256[r] is its offset (class B only on the band route).  One warp
-  // issues every peer load at once.
+  // list: sub-list 16 j + w is warp w's region in CTA j, and h256[16 j + w]
+  // its offset.  One warp issues every peer load at once.
   if (warp == 0) {
     uint32_t ca = 0u, cb = 0u;
     if (lane < P) {
       ca = ld_peer(peer_addr(smem_addr(&cs.cnt_a), (uint32_t)lane));
       cb = ld_peer(peer_addr(smem_addr(&cs.cnt_b), (uint32_t)lane));
     }
-    uint32_t c[8];
+    uint32_t c[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int rr = 8 * lane + i, j = rr >> 5, w = (rr >> 1) & 15, cls = rr & 1;
-      c[i] = 0u;
-      if (j < P)
-        c[i] = ld_peer(peer_addr(smem_addr(cls ? &cs.wcntb[w] : &cs.wcnt[w]), (uint32_t)j));
+    for (int i = 0; i < 4; ++i) {
+      const int rr = 4 * lane + i, j = rr >> 4, w = rr & 15;
+      c[i] = j < P ? ld_peer(peer_addr(smem_addr(&cs.wcnt[w]), (uint32_t)j)) : 0u;
     }
     ca = __reduce_add_sync(kFull, ca);
     cb = __reduce_add_sync(kFull, cb);
-    const bool band = !guess && p.dual && ca < (uint32_t)K;
     bool over = false;
-    uint32_t s8 = 0u;
+    uint32_t s4 = 0u;
 #pragma unroll
-    for (int i = 0; i < 8; i += 2) {
-      over = over || c[i] + c[i + 1] > (uint32_t)kRegionCap;
-      if (!band) c[i + 1] = 0u;
-      s8 += c[i] + c[i + 1];
+    for (int i = 0; i < 4; ++i) {
+      over = over || c[i] > (uint32_t)kRegionCap;
+      s4 += c[i];
     }
-    uint32_t incl = s8;
+    uint32_t incl = s4;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const uint32_t y = __shfl_up_sync(kFull, incl, o);
       if (lane >= o) incl += y;
     }
-    uint32_t run = incl - s8;
+    uint32_t run = incl - s4;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      h256[8 * lane + i] = run;
+    for (int i = 0; i < 4; ++i) {
+      h256[4 * lane + i] = run;
       run += c[i];
     }
     over = __any_sync(kFull, over);
@@ -2301,8 +2339,8 @@ __global__ void __launch_bounds__(kClusterThreads, 2) cluster_split_kernel(Param
   uint32_t k = (uint32_t)K;
   int tstar = -1, e0 = 0, q0n = 0;
   Cut cut{0, 0u, 0u, false};
-  const bool with_band = route == EXACT_TOPK_ROUTE_BAND;
-  const uint32_t nfront = with_band ? C0 + CB : C0;
+  // every admitted key is gathered; the selection ignores keys above F.hi
+  const uint32_t nfront = C0 + CB;
   const bool list_path = !recover && sc.bcast == 0 && nfront <= kMergeCap;
   if (!recover) {
     const bool with_b = route == EXACT_TOPK_ROUTE_BAND;
@@ -2316,40 +2354,34 @@ __global__ void __launch_bounds__(kClusterThreads, 2) cluster_split_kernel(Param
     // K-th smallest frontier key locally: commit the keys below it and fill
     // the rest from its ties (eqs. 22-25 reach the same threshold).
     const uint32_t total = nfront;
-    // Warp w copies sub-lists w, w + 16, ...: consecutive keys of one peer
-    // region per request, all requests of a warp in flight together.
-    const int nsub = 2 * P * kWarps;
+    // Warp w copies the regions of warp w in every CTA: consecutive keys of
+    // one peer region per request, all of a warp's requests in flight together.
     const uint32_t kb = smem_addr(keys);
-    for (int r0 = warp; r0 < nsub; r0 += 4 * kWarps) {
-      uint32_t vv[4][4];
+    uint32_t vv[kClusterMaxSplits][4];
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const int rr = r0 + b * kWarps;
+    for (int j = 0; j < kClusterMaxSplits; ++j) {
 #pragma unroll
-        for (int x = 0; x < 4; ++x) vv[b][x] = 0u;
-        if (rr < nsub) {
-          const uint32_t beg = h256[rr], end = rr + 1 < nsub ? h256[rr + 1] : total;
-          const uint32_t j = (uint32_t)(rr >> 5), w = (uint32_t)((rr >> 1) & 15);
+      for (int x = 0; x < 4; ++x) vv[j][x] = 0u;
+      if (j < P) {
+        const int rr = 16 * j + warp;
+        const uint32_t beg = h256[rr], end = rr + 1 < 16 * P ? h256[rr + 1] : total;
 #pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            const uint32_t e = (uint32_t)lane + 32u * x;
-            if (beg + e < end) {
-              const uint32_t word = w * kRegionCap + ((rr & 1) ? (uint32_t)kRegionCap - 1u - e : e);
-              vv[b][x] = ld_peer(peer_addr(kb + 4u * word, j));
-            }
-          }
+        for (int x = 0; x < 4; ++x) {
+          const uint32_t e = (uint32_t)lane + 32u * x;
+          if (beg + e < end)
+            vv[j][x] = ld_peer(peer_addr(kb + 4u * ((uint32_t)warp * kRegionCap + e), (uint32_t)j));
         }
       }
+    }
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const int rr = r0 + b * kWarps;
-        if (rr < nsub) {
-          const uint32_t beg = h256[rr], end = rr + 1 < nsub ? h256[rr + 1] : total;
+    for (int j = 0; j < kClusterMaxSplits; ++j) {
+      if (j < P) {
+        const int rr = 16 * j + warp;
+        const uint32_t beg = h256[rr], end = rr + 1 < 16 * P ? h256[rr + 1] : total;
 #pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            const uint32_t e = (uint32_t)lane + 32u * x;
-            if (beg + e < end) sumx[beg + e] = vv[b][x];
-          }
+        for (int x = 0; x < 4; ++x) {
+          const uint32_t e = (uint32_t)lane + 32u * x;
+          if (beg + e < end) sumx[beg + e] = vv[j][x];
         }
       }
     }
@@ -2405,14 +2437,14 @@ __global__ void __launch_bounds__(kClusterThreads, 2) cluster_split_kernel(Param
     // candidates: this CTA's own admitted entries (regions), frontier keys only
     // candidates: each warp visits its own region (this CTA's admitted
     // entries), frontier keys only
-    const uint32_t ca = cs.wcnt[warp];
-    const uint32_t cb = with_band ? cs.wcntb[warp] : 0u;  // ca + cb <= kRegionCap here
+    const uint32_t cw = cs.wcnt[warp];  // <= kRegionCap on this path
+    const uint32_t hiF = F.hi;
     const uint32_t* wk = keys + warp * kRegionCap;
     const uint16_t* wp = pos + warp * kRegionCap;
     auto visit = [&](auto&& fn) {
-      for (uint32_t i = lane; i < ca + cb; i += 32) {
-        const uint32_t x = i < ca ? i : (uint32_t)kRegionCap - 1u - (i - ca);
-        fn(wk[x], false, lo + (int32_t)wp[x]);
+      for (uint32_t i = lane; i < cw; i += 32) {
+        const uint32_t d = wk[i];
+        if (d <= hiF) fn(d, false, lo + (int32_t)wp[i]);
       }
     };
     cluster_commit<G>(visit, cut.commit_below, cut.tie_key, cut.ties, cut.bad, a_out, a_keep, sc,
