@@ -215,6 +215,23 @@ __device__ __forceinline__ uint32_t ld_stream1(const float* p) {
   return v;
 }
 
+// L2 prefetch of [p, p + bytes) by the TMA engine: a hint with no completion
+// to wait for.  p 16-byte aligned, bytes a positive multiple of 16, the range
+// inside one allocation.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+// Bytes of a row kept requested ahead of a complete-row pass, and of the next
+// row's head requested during a row's refinement.
+#ifndef ETK_L2_AHEAD_KB
+#define ETK_L2_AHEAD_KB 128
+#endif
+#ifndef ETK_L2_NEXT_KB
+#define ETK_L2_NEXT_KB 128
+#endif
+constexpr uint32_t kL2Ahead = ETK_L2_AHEAD_KB * 1024u;
+constexpr uint32_t kL2Next = ETK_L2_NEXT_KB * 1024u;
+
 // Asynchronous 4-byte copy global -> shared (cp.async); completion is awaited
 // with cp_async_wait_all by the issuing thread.
 __device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
@@ -608,6 +625,15 @@ __device__ __forceinline__ void scan_tiles(const float* row, int lo, int hi, uin
   q.vidx = reinterpret_cast<int32_t*>(q.vals + kQueueCap * 8);
   int qn = 0;  // warp-uniform stack depth
   const float* body = row + sp.a0;
+  // One thread keeps kL2Ahead bytes of the row requested ahead of the pass,
+  // through the TMA engine's L2 prefetch: bytes in flight from HBM that hold
+  // neither registers nor shared memory.
+  constexpr uint32_t kTileBytes = G::kThreads * 32u;  // one ring step of the group
+  const uint64_t body_bytes = (uint64_t)sp.nvec * 32u;
+  if (tid == 0 && body_bytes > 0) {
+    const uint64_t first = body_bytes < kL2Ahead ? body_bytes : kL2Ahead;
+    prefetch_l2(body, (uint32_t)first);
+  }
   constexpr uint32_t kSentinel = SIGNED_FAST ? 0x80000000u : 0xFFFFFFFFu;
   // Ring of kRing single-vector tiles: tile k of this thread is the vector
   // k * kThreads + rank; while tile k is filtered, tiles k+1 .. k+kRing-1 are
@@ -638,6 +664,13 @@ __device__ __forceinline__ void scan_tiles(const float* row, int lo, int hi, uin
         } else {
 #pragma unroll
           for (int e = 0; e < 8; ++e) dst[e] = kSentinel;
+        }
+      }
+      if (tid == 0) {
+        const uint64_t off = (uint64_t)k * kTileBytes + kL2Ahead;
+        if (off < body_bytes) {
+          const uint64_t len = body_bytes - off < kTileBytes ? body_bytes - off : kTileBytes;
+          prefetch_l2(reinterpret_cast<const unsigned char*>(body) + off, (uint32_t)len);
         }
       }
       const uint32_t* x = buf[u];
@@ -774,6 +807,174 @@ __device__ __forceinline__ void commit_warp(uint32_t* n_out, int32_t* out_row, i
 // Phase 3: prefix-commit-retain refinement (section 4.4, eqs. 22-25)
 // ----------------------------------------------------------------------------
 
+// Block-wide exclusive scan of one packed value per thread (the two 16-bit
+// halves must not carry); returns this thread's exclusive prefix and the
+// group total in `total`.
+template <class G>
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, GroupScratch& sc,
+                                                         uint32_t& total) {
+  const int tid = G::rank(), lane = tid & 31, warp = tid >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) sc.warp_sums[warp] = incl;
+  G::sync();
+  uint32_t w = lane < G::kWarps ? sc.warp_sums[lane] : 0u;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFull, w, o);
+    if (lane >= o) w += y;
+  }
+  const uint32_t before = warp ? __shfl_sync(kFull, w, warp - 1) : 0u;
+  total = __shfl_sync(kFull, w, G::kWarps - 1);
+  G::sync();  // warp_sums may be reused on return
+  return before + incl - v;
+}
+
+// Block-wide min and max of one value per thread.
+template <class G>
+__device__ __forceinline__ void block_min_max(uint32_t vmin, uint32_t vmax, GroupScratch& sc,
+                                              uint32_t& omin, uint32_t& omax) {
+  const int tid = G::rank(), lane = tid & 31, warp = tid >> 5;
+  vmin = __reduce_min_sync(kFull, vmin);
+  vmax = __reduce_max_sync(kFull, vmax);
+  if constexpr (G::kWarps <= 16) {
+    // both partials in one round: minima in warp_sums[0, 16), maxima in [16, 32)
+    if (lane == 0) {
+      sc.warp_sums[warp] = vmin;
+      sc.warp_sums[16 + warp] = vmax;
+    }
+    G::sync();
+    omin = __reduce_min_sync(kFull, lane < G::kWarps ? sc.warp_sums[lane] : 0xFFFFFFFFu);
+    omax = __reduce_max_sync(kFull, lane < G::kWarps ? sc.warp_sums[16 + lane] : 0u);
+    G::sync();
+  } else {
+    if (lane == 0) sc.warp_sums[warp] = vmin;
+    G::sync();
+    omin = __reduce_min_sync(kFull, lane < G::kWarps ? sc.warp_sums[lane] : 0xFFFFFFFFu);
+    G::sync();
+    if (lane == 0) sc.warp_sums[warp] = vmax;
+    G::sync();
+    omax = __reduce_max_sync(kFull, lane < G::kWarps ? sc.warp_sums[lane] : 0u);
+    G::sync();
+  }
+}
+
+// Histogram add by a whole warp: one shared atomic when every active lane has
+// the same bin (tie runs), one per lane otherwise.
+__device__ __forceinline__ void hist_add_same(uint32_t* hist, uint32_t bin, bool active) {
+  const uint32_t act = __ballot_sync(kFull, active);
+  if (act == 0u) return;
+  const int first = __ffs(act) - 1;
+  const uint32_t b0 = __shfl_sync(kFull, bin, first);
+  if (__ballot_sync(kFull, active && bin == b0) == act) {
+    if ((int)(threadIdx.x & 31) == first) atomicAdd(&hist[b0], (uint32_t)__popc(act));
+  } else if (active) {
+    atomicAdd(&hist[bin], 1u);
+  }
+}
+
+// The t-th smallest (1 <= t <= their count) of the values in v[0, n) that
+// are <= vhi, by radix rounds of 11-bit digits taken over the values' own
+// range [min, max] (so that clustered values still spread over the bins).
+// Returns the value and, in `below`, how many considered values are smaller;
+// `bad` when no value is considered or the counts are inconsistent.
+template <class G>
+__device__ uint32_t small_select(const uint32_t* v, uint32_t n, uint32_t vhi, uint32_t t,
+                                 uint32_t* hist, GroupScratch& sc, uint32_t& below, bool& bad) {
+  const int tid = G::rank();
+  uint32_t mn = 0xFFFFFFFFu, mx = 0u;
+  for (uint32_t i = tid; i < n; i += G::kThreads) {
+    const uint32_t x = v[i];
+    if (x <= vhi) {
+      mn = min(mn, x);
+      mx = max(mx, x);
+    }
+  }
+  uint32_t kmin, kmax;
+  block_min_max<G>(mn, mx, sc, kmin, kmax);
+  below = 0u;
+  bad = kmin > kmax;
+  if (bad) return 0u;
+  uint64_t qlo = kmin, qhi = (uint64_t)kmax + 1u;
+  const uint32_t nr = (n + 31u) & ~31u;
+  while (qhi - qlo > 1u) {
+    const int s = 64 - __clzll((long long)(qhi - qlo - 1u));
+    const int width = s < 11 ? s : 11;
+    const int shift = s - width;
+    const int nbins = (1 << width) < 128 ? 128 : (1 << width);
+    clear_hist<G>(hist, nbins);
+    G::sync();
+    for (uint32_t i = tid; i < nr; i += G::kThreads) {
+      const uint32_t x = i < n ? v[i] : 0xFFFFFFFFu;
+      const bool in = i < n && x <= vhi && (uint64_t)x >= qlo && (uint64_t)x < qhi;
+      hist_add_same(hist, in ? (uint32_t)(((uint64_t)x - qlo) >> shift) : 0u, in);
+    }
+    G::sync();
+    find_boundaries<G>(hist, sc, nbins, 1, t, 0u);
+    const int b = sc.res_bin[0];
+    const uint32_t bl = sc.res_below[0], cnt = sc.res_cnt[0];
+    if (b < 0) {
+      bad = true;
+      return 0u;
+    }
+    qlo += (uint64_t)b << shift;
+    qhi = qlo + ((uint64_t)1 << shift);
+    below += bl;
+    t -= bl;
+    if (cnt <= 32u && qhi - qlo > 1u) {
+      // At most 32 values left in the bucket: one warp ranks them directly
+      // instead of further radix rounds.
+      G::sync();  // every thread has read the finder's results
+      if (tid == 0) sc.bcast = 0;
+      G::sync();
+      uint32_t* buf = hist;  // free after the finder
+      for (uint32_t i = tid; i < n; i += G::kThreads) {
+        const uint32_t x = v[i];
+        if (x <= vhi && (uint64_t)x >= qlo && (uint64_t)x < qhi) {
+          const int slot = atomicAdd(&sc.bcast, 1);
+          if (slot < 32) buf[slot] = x;
+        }
+      }
+      G::sync();
+      if (tid < 32) {
+        const int m = min(sc.bcast, 32);
+        const bool valid = tid < m;
+        const uint32_t x = valid ? buf[tid] : 0u;
+        uint32_t less = 0u, eq = 0u;
+        for (int j = 0; j < 32; ++j) {
+          const uint32_t y = __shfl_sync(kFull, x, j);
+          if (j < m) {
+            less += y < x ? 1u : 0u;
+            eq += y == x ? 1u : 0u;
+          }
+        }
+        const uint32_t hit = __ballot_sync(kFull, valid && less < t && t <= less + eq);
+        const int src = hit ? __ffs(hit) - 1 : 0;
+        const uint32_t vx = __shfl_sync(kFull, x, src);
+        const uint32_t vl = __shfl_sync(kFull, less, src);
+        if (tid == 0) {
+          sc.res_bin[1] = hit ? 1 : -1;
+          sc.res_cnt[1] = vx;
+          sc.res_below[1] = vl;
+        }
+      }
+      G::sync();
+      if (sc.res_bin[1] < 0) {
+        bad = true;
+        return 0u;
+      }
+      below += sc.res_below[1];
+      return sc.res_cnt[1];
+    }
+  }
+  return (uint32_t)qlo;
+}
+
+
 // Phase 3 (eqs. 22-25) with the commits of every digit deferred to one final
 // pass.  Round j only needs h_j over the frontier entries whose leading digits
 // match b_0..b_{j-1} (Q_j) to find b_j = min{b : H_j(b) >= k_j} and k_{j+1} =
@@ -784,9 +985,16 @@ __device__ __forceinline__ void commit_warp(uint32_t* n_out, int32_t* out_row, i
 // frontier is only read (shared memory or its global slice), never moved.
 // Entry: frontier holds n entries (Q0), hist holds h0, k = k0 indices remain,
 // sl.n_out = |E0|.  Exit: sl.n_out == K.
+//
+// When round 0 leaves the quota open on a frontier that spilled out of shared
+// memory (tie runs, constant rows), the keys of Q_1 (at most `scap`) are
+// compacted into `scratch` and the remaining digits are resolved there with
+// small_select: the same threshold, reached without further passes over the
+// global slice.
 template <class G>
 __device__ void refine(const Frontier& F, uint32_t n, uint32_t k, uint32_t* hist,
-                       GroupScratch& sc, Slot& sl, int32_t* out_row, int K) {
+                       GroupScratch& sc, Slot& sl, int32_t* out_row, int K, uint32_t* scratch,
+                       uint32_t scap) {
   const int tid = G::rank();
   const uint32_t lt = lanemask_lt();
   const uint32_t nr = (n + 31u) & ~31u;  // whole warps visit every slot index
@@ -815,6 +1023,51 @@ __device__ void refine(const Frontier& F, uint32_t n, uint32_t k, uint32_t* hist
       break;
     }
     k -= below;
+    if (j == 0 && cnt <= scap && n > F.cap) {
+      // Q_1 = frontier keys whose digit 0 is b_0: compact them, then select
+      // the k-th smallest among them.
+      G::sync();  // every thread has read the finder's results
+      if (tid == 0) sc.bcast = 0;
+      G::sync();
+      for (uint32_t p0 = 0; p0 < nr; p0 += kRefineBatch * G::kThreads) {
+        uint32_t d[kRefineBatch];
+#pragma unroll
+        for (int bb = 0; bb < kRefineBatch; ++bb) {
+          const uint32_t pp = p0 + bb * G::kThreads + tid;
+          int32_t i;
+          d[bb] = 0xFFFFFFFFu;
+          if (pp < n) F.get(pp, i, d[bb]);
+        }
+#pragma unroll
+        for (int bb = 0; bb < kRefineBatch; ++bb) {
+          const uint32_t pp = p0 + bb * G::kThreads + tid;
+          if (p0 + bb * G::kThreads >= nr) break;  // warp-uniform
+          const bool in = pp < n && (d[bb] >> 21) == prefix;
+          const uint32_t bal = __ballot_sync(kFull, in);
+          if (bal != 0u) {
+            uint32_t base = 0u;
+            if ((tid & 31) == 0) base = (uint32_t)atomicAdd(&sc.bcast, __popc(bal));
+            base = __shfl_sync(kFull, base, 0);
+            const uint32_t slot = base + (uint32_t)__popc(bal & lt);
+            if (in && slot < scap) scratch[slot] = d[bb];
+          }
+        }
+      }
+      G::sync();
+      uint32_t below1;
+      bool bad = false;
+      const uint32_t vstar = small_select<G>(scratch, cnt, 0xFFFFFFFFu, k, hist, sc, below1, bad);
+      if (bad) {  // inconsistent counts: cannot happen; finish_row flags it
+        k = 0;
+        resolved = true;
+        break;
+      }
+      commit_below = vstar;
+      tie_key = vstar;
+      ties = k - below1;
+      resolved = true;
+      break;
+    }
     if (j == 2) {
       commit_below = prefix;  // the full key T*
       tie_key = prefix;
@@ -1226,6 +1479,16 @@ __device__ int claim_and_prefetch(const Params& p, int M, Slot& sl, GroupScratch
     if (L > p.K && nv >= qmax) {
       npre = nv < kViewPrefetch ? nv : kViewPrefetch;
       const float* row = p.logits + (int64_t)nr * p.pitch;
+      if (threadIdx.x == 0) {
+        // the head of the next row: in flight from HBM during this row's
+        // refinement (16-byte aligned range inside the row)
+        const uintptr_t b = (reinterpret_cast<uintptr_t>(row) + 15u) & ~(uintptr_t)15u;
+        const uintptr_t e = (reinterpret_cast<uintptr_t>(row) + (uintptr_t)L * 4u) & ~(uintptr_t)15u;
+        if (e > b) {
+          const uintptr_t len = e - b < kL2Next ? e - b : kL2Next;
+          prefetch_l2(reinterpret_cast<const void*>(b), (uint32_t)len);
+        }
+      }
       for (int t = threadIdx.x; t < npre; t += kPersistentThreads)
         cp_async4(view + t, row + a + (int64_t)t * p.s);
       cp_async_commit();
@@ -1323,7 +1586,8 @@ __device__ void simple_row(const Params& p, int r, Slot& sl, const Frontier& F, 
   G::sync();
   if (exact) exact_recovery<G>(p, row, L, F, hist, sc, sl, out_row, queues);
   next = claim_and_prefetch(p, M, sl, sc, view);
-  refine<G>(F, sl.n_front, (uint32_t)(K - sl.e0), hist, sc, sl, out_row, K);
+  refine<G>(F, sl.n_front, (uint32_t)(K - sl.e0), hist, sc, sl, out_row, K, queues,
+              (uint32_t)(G::kWarps * kQueueWords));
   finish_row<G>(p, sl, out_row);
   if (threadIdx.x == 0) write_slot_trace(p, sl);
 }
@@ -1380,7 +1644,8 @@ __global__ void __launch_bounds__(kRowLocalThreads, 1) row_local_exact_kernel(Pa
                                                                           sl, out_row);
       else
         exact_recovery<G>(p, row, L, F, hist, sc, sl, out_row, queues);
-      refine<G>(F, sl.n_front, (uint32_t)(K - sl.e0), hist, sc, sl, out_row, K);
+      refine<G>(F, sl.n_front, (uint32_t)(K - sl.e0), hist, sc, sl, out_row, K, queues,
+              (uint32_t)(G::kWarps * kQueueWords));
       finish_row<G>(p, sl, out_row);
       if (threadIdx.x == 0)
         write_trace(p, r, EXACT_TOPK_ROUTE_DIRECT_EXACT, -1, -1, -1, -1, sl.tstar, sl.e0, sl.q0n);
@@ -1484,7 +1749,8 @@ __global__ void __launch_bounds__(kKvSplitThreads, 2) kv_split_kernel(Params p) 
       // View unusable: the row takes the direct-exact route on one CTA.
       if (seg == 0) {
         exact_recovery<G>(p, row, L, F, hist, sc, sl, out_row, queues);
-        refine<G>(F, sl.n_front, (uint32_t)(K - sl.e0), hist, sc, sl, out_row, K);
+        refine<G>(F, sl.n_front, (uint32_t)(K - sl.e0), hist, sc, sl, out_row, K, queues,
+              (uint32_t)(G::kWarps * kQueueWords));
         finish_row<G>(p, sl, out_row);
         if (tid == 0)
           write_trace(p, r, EXACT_TOPK_ROUTE_DIRECT_EXACT, -1, -1, -1, -1, sl.tstar, sl.e0,
@@ -1625,13 +1891,15 @@ __global__ void __launch_bounds__(kKvSplitThreads, 2) kv_split_kernel(Params p) 
       G::sync();
     }
     q0n = (int)total;
-    refine<G>(F, total, (uint32_t)K, hist, sc, sl, out_row, K);
+    refine<G>(F, total, (uint32_t)K, hist, sc, sl, out_row, K, queues,
+              (uint32_t)(G::kWarps * kQueueWords));
   } else {
     exact_recovery<G>(p, row, L, F, hist, sc, sl, out_row, queues);
     tstar = sl.tstar;
     e0 = sl.e0;
     q0n = sl.q0n;
-    refine<G>(F, sl.n_front, (uint32_t)(K - e0), hist, sc, sl, out_row, K);
+    refine<G>(F, sl.n_front, (uint32_t)(K - e0), hist, sc, sl, out_row, K, queues,
+              (uint32_t)(G::kWarps * kQueueWords));
   }
   finish_row<G>(p, sl, out_row);
   if (tid == 0) write_trace(p, r, route, tau0, tau1, (int)c0, c1, tstar, e0, q0n);
@@ -1830,66 +2098,6 @@ struct Screen {
 };
 
 
-// Block-wide exclusive scan of one packed value per thread (the two 16-bit
-// halves must not carry); returns this thread's exclusive prefix and the
-// group total in `total`.
-template <class G>
-__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, GroupScratch& sc,
-                                                         uint32_t& total) {
-  const int tid = G::rank(), lane = tid & 31, warp = tid >> 5;
-  uint32_t incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(kFull, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) sc.warp_sums[warp] = incl;
-  G::sync();
-  uint32_t w = lane < G::kWarps ? sc.warp_sums[lane] : 0u;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(kFull, w, o);
-    if (lane >= o) w += y;
-  }
-  const uint32_t before = warp ? __shfl_sync(kFull, w, warp - 1) : 0u;
-  total = __shfl_sync(kFull, w, G::kWarps - 1);
-  G::sync();  // warp_sums may be reused on return
-  return before + incl - v;
-}
-
-// Block-wide min and max of one value per thread.
-template <class G>
-__device__ __forceinline__ void block_min_max(uint32_t vmin, uint32_t vmax, GroupScratch& sc,
-                                              uint32_t& omin, uint32_t& omax) {
-  const int tid = G::rank(), lane = tid & 31, warp = tid >> 5;
-  vmin = __reduce_min_sync(kFull, vmin);
-  vmax = __reduce_max_sync(kFull, vmax);
-  if (lane == 0) {
-    sc.warp_sums[warp] = vmin;
-    sc.warp_sums[16 + warp] = vmax;
-  }
-  G::sync();
-  uint32_t a = lane < G::kWarps ? sc.warp_sums[lane] : 0xFFFFFFFFu;
-  uint32_t b = lane < G::kWarps ? sc.warp_sums[16 + lane] : 0u;
-  omin = __reduce_min_sync(kFull, a);
-  omax = __reduce_max_sync(kFull, b);
-  G::sync();
-}
-
-// Histogram add by a whole warp: one shared atomic when every active lane has
-// the same bin (tie runs), one per lane otherwise.
-__device__ __forceinline__ void hist_add_same(uint32_t* hist, uint32_t bin, bool active) {
-  const uint32_t act = __ballot_sync(kFull, active);
-  if (act == 0u) return;
-  const int first = __ffs(act) - 1;
-  const uint32_t b0 = __shfl_sync(kFull, bin, first);
-  if (__ballot_sync(kFull, active && bin == b0) == act) {
-    if ((int)(threadIdx.x & 31) == first) atomicAdd(&hist[b0], (uint32_t)__popc(act));
-  } else if (active) {
-    atomicAdd(&hist[bin], 1u);
-  }
-}
-
 // Result of Phase 3: commit every frontier key below `commit_below`, then
 // `ties` keys equal to `tie_key`.
 struct Cut {
@@ -1898,103 +2106,6 @@ struct Cut {
   uint32_t ties;
   bool bad;
 };
-
-// The t-th smallest (1 <= t <= their count) of the values in v[0, n) that
-// are <= vhi, by radix rounds of 11-bit digits taken over the values' own
-// range [min, max] (so that clustered values still spread over the bins).
-// Returns the value and, in `below`, how many considered values are smaller;
-// `bad` when no value is considered or the counts are inconsistent.
-template <class G>
-__device__ uint32_t small_select(const uint32_t* v, uint32_t n, uint32_t vhi, uint32_t t,
-                                 uint32_t* hist, GroupScratch& sc, uint32_t& below, bool& bad) {
-  const int tid = G::rank();
-  uint32_t mn = 0xFFFFFFFFu, mx = 0u;
-  for (uint32_t i = tid; i < n; i += G::kThreads) {
-    const uint32_t x = v[i];
-    if (x <= vhi) {
-      mn = min(mn, x);
-      mx = max(mx, x);
-    }
-  }
-  uint32_t kmin, kmax;
-  block_min_max<G>(mn, mx, sc, kmin, kmax);
-  below = 0u;
-  bad = kmin > kmax;
-  if (bad) return 0u;
-  uint64_t qlo = kmin, qhi = (uint64_t)kmax + 1u;
-  const uint32_t nr = (n + 31u) & ~31u;
-  while (qhi - qlo > 1u) {
-    const int s = 64 - __clzll((long long)(qhi - qlo - 1u));
-    const int width = s < 11 ? s : 11;
-    const int shift = s - width;
-    const int nbins = (1 << width) < 128 ? 128 : (1 << width);
-    clear_hist<G>(hist, nbins);
-    G::sync();
-    for (uint32_t i = tid; i < nr; i += G::kThreads) {
-      const uint32_t x = i < n ? v[i] : 0xFFFFFFFFu;
-      const bool in = i < n && x <= vhi && (uint64_t)x >= qlo && (uint64_t)x < qhi;
-      hist_add_same(hist, in ? (uint32_t)(((uint64_t)x - qlo) >> shift) : 0u, in);
-    }
-    G::sync();
-    find_boundaries<G>(hist, sc, nbins, 1, t, 0u);
-    const int b = sc.res_bin[0];
-    const uint32_t bl = sc.res_below[0], cnt = sc.res_cnt[0];
-    if (b < 0) {
-      bad = true;
-      return 0u;
-    }
-    qlo += (uint64_t)b << shift;
-    qhi = qlo + ((uint64_t)1 << shift);
-    below += bl;
-    t -= bl;
-    if (cnt <= 32u && qhi - qlo > 1u) {
-      // At most 32 values left in the bucket: one warp ranks them directly
-      // instead of further radix rounds.
-      G::sync();  // every thread has read the finder's results
-      if (tid == 0) sc.bcast = 0;
-      G::sync();
-      uint32_t* buf = hist;  // free after the finder
-      for (uint32_t i = tid; i < n; i += G::kThreads) {
-        const uint32_t x = v[i];
-        if (x <= vhi && (uint64_t)x >= qlo && (uint64_t)x < qhi) {
-          const int slot = atomicAdd(&sc.bcast, 1);
-          if (slot < 32) buf[slot] = x;
-        }
-      }
-      G::sync();
-      if (tid < 32) {
-        const int m = min(sc.bcast, 32);
-        const bool valid = tid < m;
-        const uint32_t x = valid ? buf[tid] : 0u;
-        uint32_t less = 0u, eq = 0u;
-        for (int j = 0; j < 32; ++j) {
-          const uint32_t y = __shfl_sync(kFull, x, j);
-          if (j < m) {
-            less += y < x ? 1u : 0u;
-            eq += y == x ? 1u : 0u;
-          }
-        }
-        const uint32_t hit = __ballot_sync(kFull, valid && less < t && t <= less + eq);
-        const int src = hit ? __ffs(hit) - 1 : 0;
-        const uint32_t vx = __shfl_sync(kFull, x, src);
-        const uint32_t vl = __shfl_sync(kFull, less, src);
-        if (tid == 0) {
-          sc.res_bin[1] = hit ? 1 : -1;
-          sc.res_cnt[1] = vx;
-          sc.res_below[1] = vl;
-        }
-      }
-      G::sync();
-      if (sc.res_bin[1] < 0) {
-        bad = true;
-        return 0u;
-      }
-      below += sc.res_below[1];
-      return sc.res_cnt[1];
-    }
-  }
-  return (uint32_t)qlo;
-}
 
 // Phase 3 over the cluster for rows whose frontier does not fit a merged
 // list (tie-heavy rows, exact coarse recovery): 11+11+10 digits of the key,
