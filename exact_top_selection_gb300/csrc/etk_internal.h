@@ -20,7 +20,15 @@ constexpr int kCtrExit = 1;
 constexpr int kCtrStatus = 2;
 constexpr int kCtrArriveBase = 4;
 
-constexpr int kPersistentThreads = 512;
+#ifndef ETK_PERSISTENT_THREADS
+#define ETK_PERSISTENT_THREADS 512
+#endif
+#ifndef ETK_PERSISTENT_CAP
+#define ETK_PERSISTENT_CAP 4096
+#endif
+// Persistent sampled kernel: CTA size (1024 / kPersistentThreads CTAs per SM)
+// and on-chip frontier entries.
+constexpr int kPersistentThreads = ETK_PERSISTENT_THREADS;
 constexpr int kKvSplitThreads = 512;
 constexpr int kRowLocalThreads = 1024;
 constexpr int kClusterThreads = 512;
@@ -28,7 +36,7 @@ constexpr int kClusterThreads = 512;
 // the largest cluster (the portable limit).
 constexpr int kClusterStage = 16384;
 constexpr int kClusterMaxSplits = 8;
-constexpr int kPersistentCap = 4096;
+constexpr int kPersistentCap = ETK_PERSISTENT_CAP;
 constexpr int kKvSplitCap = 4096;
 constexpr int kRowLocalCap = 8192;
 // Rows of the row-local exact kernel up to this length stay in registers.

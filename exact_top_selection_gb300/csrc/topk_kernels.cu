@@ -337,7 +337,10 @@ struct Frontier {
 constexpr int kQueueCap = 64;  // < 32 before a vector slot + at most 32 pushed by it
 constexpr int kQueueWords = kQueueCap * 9;
 // View entries of the next row prefetched into shared memory (persistent kernel).
-constexpr int kViewPrefetch = 4096;
+#ifndef ETK_VIEW_PREFETCH
+#define ETK_VIEW_PREFETCH 4096
+#endif
+constexpr int kViewPrefetch = ETK_VIEW_PREFETCH;
 
 // Dynamic shared memory layouts (byte offsets), one per kernel family.
 struct SmemLayout {
@@ -400,22 +403,29 @@ __device__ __forceinline__ void clear_hist(uint32_t* hist, int nbins) {
 // complete, with a group barrier between consecutive calls; results are
 // visible to every thread of the group on return.
 //
-// nbins is a multiple of 128 with at most one 128-bin chunk per warp: warp w
-// sums chunk w (lane l holds its bins 4l .. 4l+3), and after one barrier every
-// warp scans the chunk totals, so that the warp whose chunk holds a target
-// resolves it from the registers it already has.
+// nbins is a multiple of 128 (at most 2048): warp w sums 128-bin chunks w,
+// w + warps, ... (lane l holds bins 4l .. 4l+3 of a chunk), and after one
+// barrier every warp scans the chunk totals, so that the warp whose chunk
+// holds a target resolves it from the registers it already has.
 template <class G>
 __device__ void find_boundaries(const uint32_t* hist, GroupScratch& sc, int nbins, int ntargets,
                                 uint32_t t0, uint32_t t1) {
+  constexpr int kCpw = (16 + G::kWarps - 1) / G::kWarps;  // chunks per warp (nbins <= 2048)
   const int tid = G::rank(), lane = tid & 31, warp = tid >> 5;
   const int nch = nbins >> 7;
-  uint4 v = make_uint4(0u, 0u, 0u, 0u);
-  uint32_t s4 = 0u;
-  if (warp < nch) {
-    v = reinterpret_cast<const uint4*>(hist)[warp * 32 + lane];
-    s4 = v.x + v.y + v.z + v.w;
-    const uint32_t tot = __reduce_add_sync(kFull, s4);
-    if (lane == 0) sc.warp_sums[warp] = tot;
+  uint4 v[kCpw];
+  uint32_t s4[kCpw];
+#pragma unroll
+  for (int c = 0; c < kCpw; ++c) {
+    const int ch = warp + c * G::kWarps;
+    v[c] = make_uint4(0u, 0u, 0u, 0u);
+    s4[c] = 0u;
+    if (ch < nch) {
+      v[c] = reinterpret_cast<const uint4*>(hist)[ch * 32 + lane];
+      s4[c] = v[c].x + v[c].y + v[c].z + v[c].w;
+      const uint32_t tot = __reduce_add_sync(kFull, s4[c]);
+      if (lane == 0) sc.warp_sums[ch] = tot;
+    }
   }
   G::sync();
   if (warp < nch) {
@@ -427,52 +437,57 @@ __device__ void find_boundaries(const uint32_t* hist, GroupScratch& sc, int nbin
       if (lane >= o) cincl += y;
     }
     const uint32_t grand = __shfl_sync(kFull, cincl, 31);
-    const uint32_t mine_before = __shfl_sync(kFull, cincl - ct, warp);  // before chunk `warp`
-    uint32_t incl = s4;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(kFull, incl, o);
-      if (lane >= o) incl += y;
-    }
-    const uint32_t excl = mine_before + incl - s4;
+    for (int c = 0; c < kCpw; ++c) {
+      const int ch = warp + c * G::kWarps;
+      if (ch >= nch) break;  // warp-uniform
+      const uint32_t before = __shfl_sync(kFull, cincl - ct, ch);  // before chunk ch
+      uint32_t incl = s4[c];
 #pragma unroll
-    for (int x = 0; x < 2; ++x) {
-      if (x >= ntargets) break;
-      const uint32_t t = x == 0 ? t0 : t1;
-      if (grand < t) {
-        if (warp == 0 && lane == 0) {
-          sc.res_bin[x] = -1;
-          sc.res_below[x] = grand;
-          sc.res_cnt[x] = 0u;
-        }
-        continue;
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
       }
-      if (t == 0u) {  // H(0) >= 0
-        if (warp == 0 && lane == 0) {
-          sc.res_bin[x] = 0;
-          sc.res_below[x] = 0u;
-          sc.res_cnt[x] = hist[0];
-        }
-        continue;
-      }
-      // the lane (of the chunk's warp) whose four bins cross t
-      if (excl < t && t <= excl + s4) {
-        const uint32_t h[4] = {v.x, v.y, v.z, v.w};
-        uint32_t r0 = excl;
-        int b = -1;
-        uint32_t bl = 0u, bc = 0u;
+      const uint32_t excl = before + incl - s4[c];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          if (b < 0 && r0 + h[i] >= t) {
-            b = i;
-            bl = r0;
-            bc = h[i];
+      for (int x = 0; x < 2; ++x) {
+        if (x >= ntargets) break;
+        const uint32_t t = x == 0 ? t0 : t1;
+        if (grand < t) {
+          if (warp == 0 && c == 0 && lane == 0) {
+            sc.res_bin[x] = -1;
+            sc.res_below[x] = grand;
+            sc.res_cnt[x] = 0u;
           }
-          r0 += h[i];
+          continue;
         }
-        sc.res_bin[x] = warp * 128 + lane * 4 + b;
-        sc.res_below[x] = bl;
-        sc.res_cnt[x] = bc;
+        if (t == 0u) {  // H(0) >= 0
+          if (warp == 0 && c == 0 && lane == 0) {
+            sc.res_bin[x] = 0;
+            sc.res_below[x] = 0u;
+            sc.res_cnt[x] = hist[0];
+          }
+          continue;
+        }
+        // the lane (of the chunk's warp) whose four bins cross t
+        if (excl < t && t <= excl + s4[c]) {
+          const uint32_t h[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+          uint32_t r0 = excl;
+          int b = -1;
+          uint32_t bl = 0u, bc = 0u;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            if (b < 0 && r0 + h[i] >= t) {
+              b = i;
+              bl = r0;
+              bc = h[i];
+            }
+            r0 += h[i];
+          }
+          sc.res_bin[x] = ch * 128 + lane * 4 + b;
+          sc.res_below[x] = bl;
+          sc.res_cnt[x] = bc;
+        }
       }
     }
   }
@@ -1592,7 +1607,8 @@ __device__ void simple_row(const Params& p, int r, Slot& sl, const Frontier& F, 
   if (threadIdx.x == 0) write_slot_trace(p, sl);
 }
 
-__global__ void __launch_bounds__(kPersistentThreads, 2) persistent_sampled_kernel(Params p) {
+__global__ void __launch_bounds__(kPersistentThreads, 1024 / kPersistentThreads)
+    persistent_sampled_kernel(Params p) {
   unsigned char* sm = smem_base();
   const SmemLayout lay = smem_layout(EXACT_TOPK_FAMILY_PERSISTENT_SAMPLED, p.cap);
   Slot& sl = *reinterpret_cast<Slot*>(sm + lay.slots);
@@ -2280,10 +2296,17 @@ __global__ void __launch_bounds__(kClusterThreads, 2) cluster_split_kernel(Param
                 : 0u;
   }
 
-  // ---- segment copy (TMA bulk), in flight during Phase 1 ----
+  // ---- segment copy (TMA bulk) ----
+  // Issued at once on the guess and direct routes; on the sampled route
+  // (ETK_TMA_AFTER_VIEW) only once the view's loads have returned, so that
+  // those loads do not queue behind the cluster's copies.
+#ifndef ETK_TMA_AFTER_VIEW
+#define ETK_TMA_AFTER_VIEW 0
+#endif
+  const bool copy_late = ETK_TMA_AFTER_VIEW && sampled;
   if (tid == 0) {
     mbar_init(bar, 1u);
-    if (nb > 0) bulk_copy_g2s(smem_addr(stage), src, (uint32_t)nb * 4u, bar);
+    if (nb > 0 && !copy_late) bulk_copy_g2s(smem_addr(stage), src, (uint32_t)nb * 4u, bar);
     cs.cnt_a = 0u;
     cs.cnt_b = 0u;
     cs.n_out = 0u;
@@ -2295,12 +2318,9 @@ __global__ void __launch_bounds__(kClusterThreads, 2) cluster_split_kernel(Param
   for (int t = nb + tid; t < n; t += G::kThreads) stage[t] = ld_stream1(src + t);
 
   // ---- Phase 1 ----
-  // The view is split like the row.  Each CTA publishes the coarse bins of
-  // its own view positions; every CTA gathers all of them (at most kMergeCap)
-  // and selects the q0-th and q1-th smallest bins, which are tau0 and tau1 of
-  // eq. 15 (the inclusive prefix of the view histogram first reaches q at the
-  // q-th smallest bin).  Longer views are histogrammed and summed instead.
-  // The optional guess source gathers its K scores from HBM.
+  // Every CTA histograms the whole row's view (replicated, as the KV-split of
+  // section 4.5 does) and derives tau0 / tau1 and their cutoffs; the optional
+  // guess source gathers its K scores instead.
   bool guess = false, direct = false;
   if (p.prev != nullptr && guess_bin<G>(p, row, L, r, sc, sl)) {
     guess = true;
@@ -2324,6 +2344,8 @@ __global__ void __launch_bounds__(kClusterThreads, 2) cluster_split_kernel(Param
                                       (int64_t)t * p.s))],
                 1u);
     G::sync();
+    if (copy_late && tid == 0 && nb > 0)
+      bulk_copy_g2s(smem_addr(stage), src, (uint32_t)nb * 4u, bar);
     view_cutoffs<G>(p, sum, sc, sl);
   }
   uint32_t T0 = sl.T0, T1 = sl.T1;
