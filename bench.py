@@ -316,6 +316,64 @@ def keep_busy(case, stream, seconds):
         torch.cuda.synchronize(case.device)
 
 
+def guess_series_measure(device, stream, steps=16, M=64, N=65536, K=2048, seed=20260006,
+                         rounds=5):
+    """A decode batch followed over `steps` correlated steps (the optional guess
+    source): step t passes step t-1's output as prev_topk.  The same series is
+    timed with the guess and without it (sampled view), as CUDA-graph replays
+    of the whole chain over inputs larger than L2."""
+    import torch
+
+    import exact_top_selection_gb300 as etk
+    import workloads
+    Xs, kes = workloads.decode_batch_series(M, N, K, steps, seed, device=str(device))
+    runner = etk.ExactTopK(M, N, K, device=device)
+    outs = [torch.empty(M, K, dtype=torch.int32, device=device) for _ in range(steps)]
+    traces = [torch.full((M, 8), -9, dtype=torch.int32, device=device) for _ in range(steps)]
+
+    def chain(use_guess, with_trace=False):
+        for t in range(steps):
+            prev = outs[t - 1] if (use_guess and t) else None
+            runner(Xs[t], kes[t], out=outs[t], prev_topk=prev,
+                   trace=traces[t] if with_trace else None, stream=stream)
+
+    result = {"steps": steps, "M": M, "N": N, "K": K, "drift": 0.05,
+              "footprint_bytes": steps * M * N * 4}
+    for use_guess in (True, False):
+        with torch.cuda.stream(stream):
+            chain(use_guess, with_trace=True)
+        torch.cuda.synchronize(device)
+        routes = torch.cat([tr[1:, 0] if use_guess else tr[:, 0] for tr in traces]).cpu().tolist()
+        counts = {}
+        for rt in routes:
+            nm = etk.ROUTES[rt] if 0 <= rt < len(etk.ROUTES) else str(rt)
+            counts[nm] = counts.get(nm, 0) + 1
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            chain(use_guess)
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                chain(use_guess)
+        g.replay()
+        torch.cuda.synchronize(device)
+        times = []
+        for _ in range(rounds):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+            torch.cuda.synchronize(device)
+            times.append(e0.elapsed_time(e1) / 1e3 / steps)
+        times.sort()
+        key = "guess" if use_guess else "sampled"
+        result[f"us_per_call_{key}"] = times[len(times) // 2] * 1e6
+        result[f"routes_{key}"] = counts
+    del Xs, kes
+    return result
+
+
 def e2e_measure(case, steps, warmup, stream):
     """Same metric through the public API with host buffers: per step, H2D of
     the score matrix, lengths and live count from pinned memory, the call, and
@@ -440,6 +498,10 @@ def run_ours(args):
             if c is not case:
                 del c
                 torch.cuda.empty_cache()
+    guess_series = None
+    if args.all_configs:
+        guess_series = guess_series_measure(device, stream)
+        torch.cuda.empty_cache()
     sampler.stop()
     clocks_all = sampler.summary()
 
@@ -470,6 +532,7 @@ def run_ours(args):
             "e2e": e2e,
             "cpu_baseline": cpu,
             "per_config": per_config,
+            "decode_guess_series": guess_series,
             "clocks_whole_run": clocks_all,
         }
         print(json.dumps(line))

@@ -141,6 +141,27 @@ def test_guess_source(family):
     assert tr[0, 0] == 6 and tr[3, 0] == 7
 
 
+@pytest.mark.parametrize("family", SAMPLED_FAMILIES)
+def test_guess_decode_series(family):
+    # A decode batch over correlated steps: each step's output is the next
+    # step's guess source; every step is exact and routes like the oracle.
+    M, N, K, steps = 6, 40000, 512, 4
+    Xs, kes = workloads.decode_batch_series(M, N, K, steps, seed=91, device="cpu")
+    prev = None
+    for t in range(steps):
+        X, ke = Xs[t].numpy(), kes[t].numpy()
+        out, tr, plan, ctr = run_gpu(X, ke, K, prev=prev, family=family)
+        compare_rows(X, ke, K, out)
+        assert_counters_zero(ctr)
+        _, tr_ref = oracle_trace_for_plan(X, ke, K, plan, prev=prev)
+        compare_trace(tr, tr_ref)
+        if t:
+            # rows long enough now and one step ago take a guess route
+            rows = (np.clip(ke, 0, N) > K) & (np.clip(kes[t - 1].numpy(), 0, N) > K)
+            assert np.isin(tr[rows, 0], [6, 7]).all(), tr[:, 0]
+        prev = out
+
+
 @pytest.mark.parametrize("family", FAMILIES)
 def test_live_rows_and_canary(family):
     M, N, K = 16, 9000, 100

@@ -218,6 +218,28 @@ def iid_rows(M, N, seed, device="cpu", dist="normal"):
     raise ValueError(dist)
 
 
+def decode_batch_series(M, N, K, steps, seed, device="cpu", drift=0.05):
+    """A decode batch followed over `steps` steps: indexer-like scores that drift
+    by `drift` * N(0,1) per step, lengths ~ U[K, N - steps] that grow by one
+    position per step (one new token), NaN padding beyond each length.
+
+    Returns lists (X_t, ke_t) of device tensors; step t+1 is correlated with
+    step t, which is what a previous-step Top-K guess relies on."""
+    g = _gen(device, seed)
+    X = indexer_scores(M, N, g, device)
+    ke0 = _randint(g, min(K, N), max(min(K, N), N - steps), M, device).to(torch.int32)
+    Xs, kes = [], []
+    for t in range(steps):
+        if t:
+            X = X + drift * torch.randn(M, N, generator=g, device=device, dtype=torch.float32)
+        ke_t = (ke0 + t).clamp(max=N).to(torch.int32)
+        Xt = X.clone()
+        pad_with_nan(Xt, ke_t, g)
+        Xs.append(Xt)
+        kes.append(ke_t)
+    return Xs, kes
+
+
 def decode_series(M, N, K, steps, seed, device="cpu", drift=0.05):
     """Temporally correlated decode steps: step t+1 = step t + drift * noise.
 
