@@ -210,6 +210,8 @@ class Case:
                      for _ in range(min(self.copies, 4))]
         self.nv = torch.tensor([self.M], dtype=torch.int32, device=device)
         self.l2_bytes = l2
+        # inputs are made on the default stream; calls run on other streams
+        torch.cuda.synchronize(device)
 
     def call(self, i, stream=None):
         return self.runner(self.X[i % self.copies], self.ke, num_valid_rows=self.nv,
@@ -328,6 +330,7 @@ def guess_series_measure(device, stream, steps=16, M=64, N=65536, K=2048, seed=2
     import workloads
     Xs, kes = workloads.decode_batch_series(M, N, K, steps, seed, device=str(device))
     runner = etk.ExactTopK(M, N, K, device=device)
+    torch.cuda.synchronize(device)  # inputs come from the default stream
     outs = [torch.empty(M, K, dtype=torch.int32, device=device) for _ in range(steps)]
     traces = [torch.full((M, 8), -9, dtype=torch.int32, device=device) for _ in range(steps)]
 
@@ -372,6 +375,132 @@ def guess_series_measure(device, stream, steps=16, M=64, N=65536, K=2048, seed=2
         result[f"routes_{key}"] = counts
     del Xs, kes
     return result
+
+
+def _time_calls(runner, Xs, ke, stream, calls=64, rounds=5, trace=None):
+    """Median per-call seconds of graph replays cycling over the inputs Xs."""
+    import torch
+    out = torch.empty(runner.plan.num_rows, runner.plan.top_k, dtype=torch.int32,
+                      device=Xs[0].device)
+    if trace is not None:
+        with torch.cuda.stream(stream):
+            runner(Xs[0], ke, out=out, trace=trace, stream=stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        runner(Xs[0], ke, out=out, stream=stream)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for c in range(calls):
+                runner(Xs[c % len(Xs)], ke, out=out, stream=stream)
+    g.replay()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(rounds):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) / 1e3 / calls)
+    times.sort()
+    return times[len(times) // 2]
+
+
+def _route_stats(trace, K):
+    import exact_top_selection_gb300 as etk
+    tr = trace.cpu().numpy()
+    routes = tr[:, 0]
+    live = routes != 0
+    n = max(1, int(live.sum()))
+    counts = {}
+    for rt in routes.tolist():
+        nm = etk.ROUTES[rt] if 0 <= rt < len(etk.ROUTES) else str(rt)
+        counts[nm] = counts.get(nm, 0) + 1
+    band = sum(counts.get(k, 0) for k in ("band", "exact_after_band"))
+    exact = sum(counts.get(k, 0) for k in ("exact_after_band", "exact_no_band", "direct_exact"))
+    c0 = tr[live & (tr[:, 3] >= 0), 3]
+    return {"routes": counts, "p_band": band / n, "p_exact": exact / n,
+            "mean_c0_over_K": float(c0.mean()) / K if c0.size else None}
+
+
+def run_sweep(args):
+    """Planner studies on one GPU: one JSON line per
+    point.  crossover: row width N against the row-local exact kernel and the
+    two sampled policies; margins: retention margin rho and view stride s on
+    prefill-shaped rows, with route rates; splits: KV-split segment count P on
+    the few-long-rows workload."""
+    import math
+
+    import torch
+
+    import exact_top_selection_gb300 as etk
+    import workloads
+    device = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.Stream(device)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+
+    def copies_for(X):
+        per = X.numel() * 4
+        c = max(1, math.ceil(4 * l2 / per)) if per < 2 * l2 else 1
+        out = [X] + [X.clone() for _ in range(c - 1)]
+        torch.cuda.synchronize(device)  # made on the default stream, read on `stream`
+        return out
+
+    def emit(d):
+        print(json.dumps(d), flush=True)
+
+    K = 2048
+    if args.sweep == "crossover":
+        M = 1024
+        for N in (8192, 12288, 16384, 24576, 32768, 49152, 65536, 98304, 131072):
+            # full-length indexer-like rows (no padding inside the prefix)
+            X = workloads.indexer_scores(M, N, workloads._gen(str(device), 20260010 + N),
+                                         str(device))
+            ke = torch.full((M,), N, dtype=torch.int32, device=device)
+            Xs = copies_for(X)
+            for name, kw in (("row_local_exact", dict(family=etk.FAMILY_ROW_LOCAL_EXACT)),
+                             ("persistent_s64_primary", dict(family=etk.FAMILY_PERSISTENT_SAMPLED,
+                                                             stride=64, dual=0)),
+                             ("persistent_s128_dual", dict(family=etk.FAMILY_PERSISTENT_SAMPLED,
+                                                           stride=128, dual=1))):
+                runner = etk.ExactTopK(M, N, K, device=device, **kw)
+                tr = torch.full((M, 8), -9, dtype=torch.int32, device=device)
+                sec = _time_calls(runner, Xs, ke, stream, trace=tr)
+                emit({"sweep": "crossover", "M": M, "N": N, "K": K, "policy": name,
+                      "us_per_call": sec * 1e6, "gbs": (M * N * 4 + M * K * 4) / sec / 1e9,
+                      **_route_stats(tr, K)})
+            del X, Xs
+            torch.cuda.empty_cache()
+    elif args.sweep == "margins":
+        M, N = 1024, 131072
+        X, ke, _ = workloads.generate("prefill_causal", M=M, N=N, K=K, device=str(device))
+        Xs = [X]
+        torch.cuda.synchronize(device)
+        alg = int(ke.to(torch.int64).clamp(0, N).sum().item()) * 4 + M * K * 4
+        for s in (64, 128, 256):
+            for rho in ((5, 4), (3, 2), (2, 1)):
+                rho1 = (rho[0] * 4 + rho[1], rho[1] * 4)  # rho + 1/4
+                runner = etk.ExactTopK(M, N, K, device=device,
+                                       family=etk.FAMILY_PERSISTENT_SAMPLED, stride=s, dual=1,
+                                       rho0=rho, rho1=rho1)
+                tr = torch.full((M, 8), -9, dtype=torch.int32, device=device)
+                sec = _time_calls(runner, Xs, ke, stream, trace=tr)
+                emit({"sweep": "margins", "M": M, "N": N, "K": K, "stride": s,
+                      "rho0": rho[0] / rho[1], "rho1": rho1[0] / rho1[1],
+                      "us_per_call": sec * 1e6, "gbs": alg / sec / 1e9, **_route_stats(tr, K)})
+    elif args.sweep == "splits":
+        X, ke, _ = workloads.generate("long_decode", device=str(device))
+        M, N = X.shape
+        Xs = copies_for(X)
+        alg = int(ke.to(torch.int64).clamp(0, N).sum().item()) * 4 + M * K * 4
+        for P in (8, 16, 32, 64):
+            runner = etk.ExactTopK(M, N, K, device=device, family=etk.FAMILY_KV_SPLIT, splits=P)
+            tr = torch.full((M, 8), -9, dtype=torch.int32, device=device)
+            sec = _time_calls(runner, Xs, ke, stream, trace=tr)
+            emit({"sweep": "splits", "M": M, "N": N, "K": K, "splits": P,
+                  "us_per_call": sec * 1e6, "gbs": alg / sec / 1e9, **_route_stats(tr, K)})
 
 
 def e2e_measure(case, steps, warmup, stream):
@@ -602,6 +731,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-seconds", type=float, default=60.0)
+    ap.add_argument("--sweep", choices=["crossover", "margins", "splits"], default=None,
+                    help="planner study instead of the bench line (one JSON line per point)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -617,7 +748,10 @@ def main(argv=None):
     else:
         import __graft_entry__
         __graft_entry__.build()
-        run_ours(args)
+        if args.sweep:
+            run_sweep(args)
+        else:
+            run_ours(args)
 
 
 if __name__ == "__main__":

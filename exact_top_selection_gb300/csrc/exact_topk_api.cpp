@@ -151,14 +151,15 @@ int exact_topk_make_plan(int64_t num_rows, int64_t max_kv_len, int64_t row_pitch
   p.sm_count = info->sm_count;
 
   // Family (section 5.5, Fig. 6): row-local exact below the sampling
-  // crossover (section 6.4: exact proposals win at 16-24K columns, sampling
-  // wins at 64K); when rows cannot fill the device, the cluster split if a
+  // crossover (section 6.4 places it between 16-24K and 64K columns on H20;
+  // on GB300 the sampled path already wins at 16K, K = 2048); when rows
+  // cannot fill the device, the cluster split if a
   // row fits the shared memory of one cluster (and its CTAs fit in about
   // two waves), else the KV-split; persistent sampled otherwise.
   const int64_t cluster_P = ceil_div64(max_kv_len, kClusterStage);
   int family = r.family;
   if (family == EXACT_TOPK_FAMILY_AUTO) {
-    if (max_kv_len < 32768)
+    if (max_kv_len < 16384)
       family = EXACT_TOPK_FAMILY_ROW_LOCAL_EXACT;
     else if (num_rows < info->sm_count)
       family = (cluster_P <= kClusterMaxSplits && info->cluster_ctas_per_sm > 0 &&
@@ -218,12 +219,13 @@ int exact_topk_make_plan(int64_t num_rows, int64_t max_kv_len, int64_t row_pitch
   if (ctas_per_sm < 1) ctas_per_sm = 1;
 
   if (family == EXACT_TOPK_FAMILY_KV_SPLIT) {
-    // P: enough segment CTAs to cover about half the device's resident CTA
-    // slots, with segments of at least 8K scores (section 4.6: KV-split trades
-    // replicated view work, R_eq = 1 + P/s, for a shorter validation span).
+    // P: enough segment CTAs to cover about a quarter of the device's resident
+    // CTA slots, with segments of at least 8K scores (section 4.6: KV-split
+    // trades replicated view work, R_eq = 1 + P/s, for a shorter validation
+    // span; on GB300 the few-long-rows workload is fastest at this P).
     int64_t P = r.splits;
     if (P == 0) {
-      const int64_t target = (int64_t)info->sm_count * ctas_per_sm / 2;
+      const int64_t target = (int64_t)info->sm_count * ctas_per_sm / 4;
       P = 1;
       while (P < 64 && num_rows * P < target) P *= 2;
       while (P > 1 && max_kv_len / P < 8192) P /= 2;
