@@ -45,9 +45,13 @@ namespace {
 
 constexpr int kCoarseBins = 2048;
 constexpr int kMaxSplits = 128;
-// Depth of each thread's ring of 256-bit loads in a complete-row pass.
+// Depth of each thread's ring of 256-bit loads in a complete-row pass.  Three
+// (two vectors in flight while one is filtered) measured faster than four in
+// the persistent kernel on GB300: at 64 registers a thread the fourth vector
+// makes the kernel spill, and the TMA L2 prefetch ahead of the pass already
+// keeps bytes in flight that hold no registers.
 #ifndef ETK_RING
-#define ETK_RING 4
+#define ETK_RING 3
 #endif
 constexpr int kRing = ETK_RING;
 constexpr uint32_t kDescPosInf = 0x007FFFFFu;  // kappa_down32(+inf)
@@ -66,6 +70,22 @@ struct CtaGroup {
   static_assert(THREADS % 32 == 0 && kWarps <= 32, "whole warps, at most 32");
   __device__ __forceinline__ static int rank() { return (int)threadIdx.x; }
   __device__ __forceinline__ static void sync() { __syncthreads(); }
+};
+
+// Warps FIRST_WARP .. FIRST_WARP + THREADS/32 - 1 of the CTA, synchronised by
+// the named barrier BAR (never 0, which __syncthreads uses).  Two such groups
+// with different barriers run different phases at the same time; every
+// function they call synchronises through G::sync() only.
+template <int THREADS, int FIRST_WARP, int BAR>
+struct SubGroup {
+  static constexpr int kThreads = THREADS;
+  static constexpr int kWarps = THREADS / 32;
+  static_assert(THREADS % 32 == 0 && kWarps <= 32, "whole warps, at most 32");
+  static_assert(BAR > 0 && BAR < 16, "a named barrier other than 0");
+  __device__ __forceinline__ static int rank() { return (int)threadIdx.x - FIRST_WARP * 32; }
+  __device__ __forceinline__ static void sync() {
+    asm volatile("bar.sync %0, %1;" ::"n"(BAR), "n"(THREADS) : "memory");
+  }
 };
 
 // ----------------------------------------------------------------------------
@@ -232,17 +252,6 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
 constexpr uint32_t kL2Ahead = ETK_L2_AHEAD_KB * 1024u;
 constexpr uint32_t kL2Next = ETK_L2_NEXT_KB * 1024u;
 
-// Asynchronous 4-byte copy global -> shared (cp.async); completion is awaited
-// with cp_async_wait_all by the issuing thread.
-__device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
-  const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(sa), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
 // ----------------------------------------------------------------------------
 // Shared state
 // ----------------------------------------------------------------------------
@@ -273,9 +282,7 @@ struct Slot {
   int32_t c0, c1, tstar, e0, q0n;
   uint32_t seg_c0, seg_cb;  // KV-split: this segment's counts
   int32_t is_last;
-  int32_t pf_row;  // persistent: row whose view sits in the prefetch buffer, or -1
-  int32_t pf_n;    // number of prefetched view entries
-  int32_t pad_[1];
+  int32_t pad_[3];
 };
 
 struct Params {
@@ -336,30 +343,35 @@ struct Frontier {
 // kQueueCap entries of 8 bit patterns plus the vector's index in the pass.
 constexpr int kQueueCap = 64;  // < 32 before a vector slot + at most 32 pushed by it
 constexpr int kQueueWords = kQueueCap * 9;
-// View entries of the next row prefetched into shared memory (persistent kernel).
-#ifndef ETK_VIEW_PREFETCH
-#define ETK_VIEW_PREFETCH 4096
+// Persistent kernel: warps [0, kRefineWarps) refine the row just classified
+// while the remaining warps claim the next row and run its Phase 1.
+#ifndef ETK_PREPARE_WARPS
+#define ETK_PREPARE_WARPS (kPersistentThreads / 128)
 #endif
-constexpr int kViewPrefetch = ETK_VIEW_PREFETCH;
+constexpr int kRefineWarps = kPersistentThreads / 32 - ETK_PREPARE_WARPS;
+static_assert(kRefineWarps > 0 && kRefineWarps < kPersistentThreads / 32,
+              "both groups need at least one warp");
 
 // Dynamic shared memory layouts (byte offsets), one per kernel family.
 struct SmemLayout {
   uint32_t slots;     // Slot[nslots]
   uint32_t scratch;   // GroupScratch[2]
   uint32_t hist;      // uint32[nslots][2048]
-  uint32_t frontier;  // uint2[nslots][cap]
+  uint32_t frontier;  // uint2[cap]
   uint32_t runs;      // KV-split run table, or 0
-  uint32_t view;      // persistent: prefetched view of the next row, or 0
   uint32_t queues;    // uint32[warps][kQueueWords]
   uint32_t total;
 };
 
 __host__ __device__ constexpr uint32_t align16(uint32_t v) { return (v + 15u) & ~15u; }
 
-__host__ __device__ inline SmemLayout smem_layout(int family, int cap) {
+// constexpr: each kernel passes its family's fixed candidate capacity, so the
+// offsets are compile-time constants.
+__host__ __device__ constexpr SmemLayout smem_layout(int family, int cap) {
   SmemLayout l{};
   const bool pers = family == EXACT_TOPK_FAMILY_PERSISTENT_SAMPLED;
-  const int nslots = 1;
+  // persistent: a second slot and histogram hold the next row's Phase 1
+  const int nslots = pers ? 2 : 1;
   const int qwarps = pers ? kPersistentThreads / 32
                           : (family == EXACT_TOPK_FAMILY_KV_SPLIT ? kKvSplitThreads / 32
                                                                   : kRowLocalThreads / 32);
@@ -371,11 +383,9 @@ __host__ __device__ inline SmemLayout smem_layout(int family, int cap) {
   l.hist = o;
   o = align16(o + nslots * kCoarseBins * 4u);
   l.frontier = o;
-  o = align16(o + nslots * (uint32_t)cap * 8u);
+  o = align16(o + (uint32_t)cap * 8u);
   l.runs = family == EXACT_TOPK_FAMILY_KV_SPLIT ? o : 0u;
   if (family == EXACT_TOPK_FAMILY_KV_SPLIT) o = align16(o + (3 * kMaxSplits + 1) * 4u);
-  l.view = pers ? o : 0u;
-  if (pers) o = align16(o + kViewPrefetch * 4u);
   l.queues = o;
   o = align16(o + qwarps * kQueueWords * 4u);
   l.total = o;
@@ -1364,17 +1374,10 @@ __device__ void view_cutoffs(const Params& p, const uint32_t* hist, GroupScratch
 // loads before using any.  Entered with a cleared histogram; leaves it dirty.
 template <class G>
 __device__ void sample_view(const Params& p, const float* row, int L, int a, uint32_t* hist,
-                            GroupScratch& sc, Slot& sl, const uint32_t* pre = nullptr,
-                            int npre = 0) {
+                            GroupScratch& sc, Slot& sl) {
   const int nv = view_size(L, a, p.s);
   const int tid = G::rank();
-  // Entries [0, npre) were copied to `pre` by this same thread layout
-  // (entry t by rank t mod kThreads), so each thread reads only its own.
-  if (npre > 0) {
-    cp_async_wait_all();
-    for (int t = tid; t < npre; t += G::kThreads) atomicAdd(&hist[coarse_bin(pre[t])], 1u);
-  }
-  for (int t0 = npre; t0 < nv; t0 += 8 * G::kThreads) {
+  for (int t0 = 0; t0 < nv; t0 += 8 * G::kThreads) {
     uint32_t u[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
@@ -1473,101 +1476,119 @@ __device__ void exit_protocol(int32_t* counters) {
 // Phase 1, the complete-row pass with its certification (band rescue, exact
 // coarse recovery), and Phase 3.  Rows after the first wave are claimed from a
 // device counter in completion order.
-// Claims the next row (in completion order: load balance across the grid)
-// and starts copying its view (Phase 1 input) into shared memory, so that the
-// copies overlap this row's refinement.
-__device__ int claim_and_prefetch(const Params& p, int M, Slot& sl, GroupScratch& sc,
-                                  uint32_t* view) {
-  if (threadIdx.x == 0) {
-    const int nr = (int)gridDim.x + atomicAdd(p.counters + kCtrQueue, 1);
+//
+// The work of a row that is not a pass over the row is split between two warp
+// groups that run at the same time: warps [0, kRefineWarps) refine and commit
+// the row just classified, while the other warps claim the next row and run
+// its Phase 1 (view histogram, boundaries and cutoffs, or the guess source)
+// into a second slot and histogram.  The next row's complete-row pass then
+// starts as soon as both groups are done.
+
+// What Phase 1 left for a claimed row (Slot::route of the next-row slot).
+constexpr int kNextNone = -1;    // the queue is exhausted
+constexpr int kNextPad = 0;      // L <= K: padded output, no selection
+constexpr int kNextSampled = 1;  // view cutoffs T0 (and T1) in the slot
+constexpr int kNextDirect = 2;   // view too small: exact coarse recovery
+constexpr int kNextGuess = 3;    // guess-source cutoff T0 in the slot
+
+// Claims a row (or takes `assigned`) and runs its Phase 1 by group V into
+// `nx`, with `vh` as the view histogram.  The caller publishes `nx` with a CTA
+// barrier.
+template <class V>
+__device__ void prepare_row(const Params& p, int M, int assigned, Slot& nx, uint32_t* vh,
+                            GroupScratch& sc) {
+  if (V::rank() == 0) {
+    const int nr = assigned >= 0 ? assigned : (int)gridDim.x + atomicAdd(p.counters + kCtrQueue, 1);
     sc.bcast = nr;
     sc.bcast2 = nr < M ? row_length(p, nr) : 0;
   }
-  __syncthreads();
-  const int nr = sc.bcast;
-  int npre = 0;
-  if (nr < M && p.prev == nullptr) {
-    const int L = sc.bcast2;
-    const int a = view_phase(nr, p.s, p.s_bits);
-    const int nv = view_size(L, a, p.s);
-    const int qmax = p.dual ? p.q1 : p.q0;
-    if (L > p.K && nv >= qmax) {
-      npre = nv < kViewPrefetch ? nv : kViewPrefetch;
-      const float* row = p.logits + (int64_t)nr * p.pitch;
-      if (threadIdx.x == 0) {
-        // the head of the next row: in flight from HBM during this row's
-        // refinement (16-byte aligned range inside the row)
-        const uintptr_t b = (reinterpret_cast<uintptr_t>(row) + 15u) & ~(uintptr_t)15u;
-        const uintptr_t e = (reinterpret_cast<uintptr_t>(row) + (uintptr_t)L * 4u) & ~(uintptr_t)15u;
-        if (e > b) {
-          const uintptr_t len = e - b < kL2Next ? e - b : kL2Next;
-          prefetch_l2(reinterpret_cast<const void*>(b), (uint32_t)len);
-        }
+  V::sync();
+  const int nr = sc.bcast, L = sc.bcast2;
+  int kind;
+  if (nr >= M) {
+    kind = kNextNone;
+  } else if (L <= p.K) {
+    kind = kNextPad;
+  } else {
+    const float* row = p.logits + (int64_t)nr * p.pitch;
+    if (V::rank() == 0) {
+      // the head of the row: in flight from HBM before its complete-row pass
+      // (16-byte aligned range inside the row)
+      const uintptr_t b = (reinterpret_cast<uintptr_t>(row) + 15u) & ~(uintptr_t)15u;
+      const uintptr_t e = (reinterpret_cast<uintptr_t>(row) + (uintptr_t)L * 4u) & ~(uintptr_t)15u;
+      if (e > b) {
+        const uintptr_t len = e - b < kL2Next ? e - b : kL2Next;
+        prefetch_l2(reinterpret_cast<const void*>(b), (uint32_t)len);
       }
-      for (int t = threadIdx.x; t < npre; t += kPersistentThreads)
-        cp_async4(view + t, row + a + (int64_t)t * p.s);
-      cp_async_commit();
+    }
+    if (p.prev != nullptr && guess_bin<V>(p, row, L, nr, sc, nx)) {
+      kind = kNextGuess;
+    } else {
+      const int a = view_phase(nr, p.s, p.s_bits);
+      if (view_size(L, a, p.s) >= (p.dual ? p.q1 : p.q0)) {
+        clear_hist<V>(vh, 2048);
+        V::sync();
+        sample_view<V>(p, row, L, a, vh, sc, nx);
+        kind = kNextSampled;
+      } else {
+        kind = kNextDirect;
+      }
     }
   }
-  __syncthreads();  // everyone has read bcast
-  if (threadIdx.x == 0) {
-    sl.pf_row = npre > 0 ? nr : -1;
-    sl.pf_n = npre;
+  if (V::rank() == 0) {
+    nx.row = nr;
+    nx.L = L;
+    nx.route = kind;
   }
-  return nr;
 }
 
-__device__ void simple_row(const Params& p, int r, Slot& sl, const Frontier& F, uint32_t* hist,
-                           GroupScratch& sc, uint32_t* queues, uint32_t* view, int M,
-                           int& next) {
+// One row whose Phase 1 sits in `nx`; on return `nx` holds the next row's.
+// Entered and left at a CTA barrier.
+__device__ void persistent_row(const Params& p, int M, Slot& sl, Slot& nx, const Frontier& F,
+                               uint32_t* hist, uint32_t* vhist, GroupScratch* sc2,
+                               uint32_t* queues) {
   using G = CtaGroup<kPersistentThreads>;
+  using R = SubGroup<kRefineWarps * 32, 0, 1>;
+  using V = SubGroup<kPersistentThreads - kRefineWarps * 32, kRefineWarps, 2>;
+  GroupScratch& sc = sc2[0];
   const int K = p.K;
+  const int r = nx.row, L = nx.L, kind = nx.route;
+  const uint32_t T0 = nx.T0, T1 = nx.T1;
+  const int tau0 = nx.tau0, tau1 = nx.tau1;
   const float* row = p.logits + (int64_t)r * p.pitch;
-  const int L = row_length(p, r);
   int32_t* out_row = p.out + (int64_t)r * K;
-  const bool have_pf = sl.pf_row == r;
-  const int npre = have_pf ? sl.pf_n : 0;
-  if (L <= K) {
-    write_pad_row<G>(out_row, L, K);
-    if (threadIdx.x == 0) write_trace(p, r, EXACT_TOPK_ROUTE_PAD, -1, -1, -1, -1, -1, -1, -1);
-    next = claim_and_prefetch(p, M, sl, sc, view);
-    return;
-  }
-  G::sync();  // every thread has read the prefetch record
-  clear_hist<G>(hist, 2048);
+  if (kind != kNextPad) clear_hist<G>(hist, 2048);
   if (threadIdx.x == 0) {
     sl.row = r;
     sl.L = L;
     sl.n_front = 0u;
     sl.n_out = 0u;
     sl.n_drop = 0u;
-    sl.tau0 = -1;
-    sl.tau1 = -1;
+    sl.T0 = T0;
+    sl.T1 = T1;
+    sl.tau0 = kind == kNextSampled || kind == kNextGuess ? tau0 : -1;
+    sl.tau1 = kind == kNextSampled ? tau1 : -1;
     sl.c0 = -1;
     sl.c1 = -1;
     sl.tstar = -1;
     sl.e0 = 0;
   }
-  G::sync();
-  FrontierSink front_sink{{}, F, hist};
-  DropSink drop;
-  bool exact = false;
-  int route;
-  if (p.prev != nullptr && guess_bin<G>(p, row, L, r, sc, sl)) {
-    const uint32_t T = sl.T0;
-    scan_two_class<G>(row, 0, L, T, T, false, &sl.n_drop, &sl.n_front, queues, drop, front_sink);
-    G::sync();
-    const uint32_t c0 = sl.n_front;
-    route = c0 >= (uint32_t)K ? EXACT_TOPK_ROUTE_GUESS : EXACT_TOPK_ROUTE_GUESS_EXACT;
-    if (threadIdx.x == 0) sl.c0 = (int)c0;
+  __syncthreads();  // every thread has read nx; the next row's group may overwrite it
+  if (kind == kNextPad) {
+    write_pad_row<G>(out_row, L, K);
+    if (threadIdx.x == 0) write_trace(p, r, EXACT_TOPK_ROUTE_PAD, -1, -1, -1, -1, -1, -1, -1);
   } else {
-    const int a = view_phase(r, p.s, p.s_bits);
-    const int qmax = p.dual ? p.q1 : p.q0;
-    if (view_size(L, a, p.s) >= qmax) {
-      sample_view<G>(p, row, L, a, hist, sc, sl, view, npre);
-      const uint32_t T0 = sl.T0, T1 = sl.T1;
-      clear_hist<G>(hist, 2048);
+    FrontierSink front_sink{{}, F, hist};
+    DropSink drop;
+    int route;
+    if (kind == kNextGuess) {
+      scan_two_class<G>(row, 0, L, T0, T0, false, &sl.n_drop, &sl.n_front, queues, drop,
+                        front_sink);
       G::sync();
+      const uint32_t c0 = sl.n_front;
+      route = c0 >= (uint32_t)K ? EXACT_TOPK_ROUTE_GUESS : EXACT_TOPK_ROUTE_GUESS_EXACT;
+      if (threadIdx.x == 0) sl.c0 = (int)c0;
+    } else if (kind == kNextSampled) {
       // Phase 2: admit d <= T0, persist candidates, build h0 (eqs. 16-17).
       scan_two_class<G>(row, 0, L, T0, T0, false, &sl.n_drop, &sl.n_front, queues, drop,
                         front_sink);
@@ -1591,43 +1612,59 @@ __device__ void simple_row(const Params& p, int r, Slot& sl, const Frontier& F, 
     } else {
       route = EXACT_TOPK_ROUTE_DIRECT_EXACT;
     }
+    const bool exact =
+        route == EXACT_TOPK_ROUTE_EXACT_AFTER_BAND || route == EXACT_TOPK_ROUTE_EXACT_NO_BAND ||
+        route == EXACT_TOPK_ROUTE_GUESS_EXACT || route == EXACT_TOPK_ROUTE_DIRECT_EXACT;
+    if (threadIdx.x == 0) {
+      sl.route = route;
+      sl.q0n = (int)sl.n_front;  // eq. 21: E0 = {}, Q0 = A(tau), k0 = K
+    }
+    G::sync();
+    if (exact) exact_recovery<G>(p, row, L, F, hist, sc, sl, out_row, queues);
   }
-  exact = route == EXACT_TOPK_ROUTE_EXACT_AFTER_BAND || route == EXACT_TOPK_ROUTE_EXACT_NO_BAND ||
-          route == EXACT_TOPK_ROUTE_GUESS_EXACT || route == EXACT_TOPK_ROUTE_DIRECT_EXACT;
-  if (threadIdx.x == 0) {
-    sl.route = route;
-    sl.q0n = (int)sl.n_front;  // eq. 21: E0 = {}, Q0 = A(tau), k0 = K
+  // Phase 3 of this row and Phase 1 of the next: side by side when the
+  // frontier is in shared memory; one after the other, each by the whole CTA,
+  // when it spilled (refinement then streams the global slice and wants every
+  // warp) or when there is nothing to refine.
+  const bool split = kind != kNextPad && sl.n_front <= F.cap;
+  if (split) {
+    if ((int)(threadIdx.x >> 5) < kRefineWarps) {
+      refine<R>(F, sl.n_front, (uint32_t)(K - sl.e0), hist, sc, sl, out_row, K, queues,
+                (uint32_t)(R::kWarps * kQueueWords));
+      finish_row<R>(p, sl, out_row);
+      if (threadIdx.x == 0) write_slot_trace(p, sl);
+    } else {
+      prepare_row<V>(p, M, -1, nx, vhist, sc2[1]);
+    }
+  } else {
+    if (kind != kNextPad) {
+      refine<G>(F, sl.n_front, (uint32_t)(K - sl.e0), hist, sc, sl, out_row, K, queues,
+                (uint32_t)(G::kWarps * kQueueWords));
+      finish_row<G>(p, sl, out_row);
+      if (threadIdx.x == 0) write_slot_trace(p, sl);
+    }
+    prepare_row<G>(p, M, -1, nx, vhist, sc2[1]);
   }
-  G::sync();
-  if (exact) exact_recovery<G>(p, row, L, F, hist, sc, sl, out_row, queues);
-  next = claim_and_prefetch(p, M, sl, sc, view);
-  refine<G>(F, sl.n_front, (uint32_t)(K - sl.e0), hist, sc, sl, out_row, K, queues,
-              (uint32_t)(G::kWarps * kQueueWords));
-  finish_row<G>(p, sl, out_row);
-  if (threadIdx.x == 0) write_slot_trace(p, sl);
+  __syncthreads();
 }
 
 __global__ void __launch_bounds__(kPersistentThreads, 1024 / kPersistentThreads)
     persistent_sampled_kernel(Params p) {
   unsigned char* sm = smem_base();
-  const SmemLayout lay = smem_layout(EXACT_TOPK_FAMILY_PERSISTENT_SAMPLED, p.cap);
-  Slot& sl = *reinterpret_cast<Slot*>(sm + lay.slots);
-  GroupScratch& sc = *reinterpret_cast<GroupScratch*>(sm + lay.scratch);
+  constexpr SmemLayout lay = smem_layout(EXACT_TOPK_FAMILY_PERSISTENT_SAMPLED, kPersistentCap);
+  Slot* slots = reinterpret_cast<Slot*>(sm + lay.slots);  // [0] this row, [1] the next
+  GroupScratch* sc2 = reinterpret_cast<GroupScratch*>(sm + lay.scratch);
   uint32_t* hist = reinterpret_cast<uint32_t*>(sm + lay.hist);
+  uint32_t* vhist = hist + kCoarseBins;
   uint32_t* queues = reinterpret_cast<uint32_t*>(sm + lay.queues);
-  uint32_t* view = reinterpret_cast<uint32_t*>(sm + lay.view);
   const Frontier F = make_frontier(p, reinterpret_cast<uint2*>(sm + lay.frontier), blockIdx.x);
   const int M = live_rows(p);
-  if (threadIdx.x == 0) sl.pf_row = -1;
-  __syncthreads();
-  int r = blockIdx.x;
-  while (r < M) {
-    int next = M;
-    simple_row(p, r, sl, F, hist, sc, queues, view, M, next);
+  if ((int)blockIdx.x < M) {  // CTA-uniform
+    prepare_row<CtaGroup<kPersistentThreads>>(p, M, (int)blockIdx.x, slots[1], vhist, sc2[1]);
     __syncthreads();
-    r = next;
+    while (slots[1].route != kNextNone)
+      persistent_row(p, M, slots[0], slots[1], F, hist, vhist, sc2, queues);
   }
-  cp_async_wait_all();  // no copy may be left in flight at exit
   exit_protocol(p.counters);
 }
 
@@ -1638,7 +1675,7 @@ __global__ void __launch_bounds__(kPersistentThreads, 1024 / kPersistentThreads)
 __global__ void __launch_bounds__(kRowLocalThreads, 1) row_local_exact_kernel(Params p) {
   using G = CtaGroup<kRowLocalThreads>;
   unsigned char* sm = smem_base();
-  const SmemLayout lay = smem_layout(EXACT_TOPK_FAMILY_ROW_LOCAL_EXACT, p.cap);
+  constexpr SmemLayout lay = smem_layout(EXACT_TOPK_FAMILY_ROW_LOCAL_EXACT, kRowLocalCap);
   Slot& sl = *reinterpret_cast<Slot*>(sm + lay.slots);
   GroupScratch& sc = *reinterpret_cast<GroupScratch*>(sm + lay.scratch);
   uint32_t* hist = reinterpret_cast<uint32_t*>(sm + lay.hist);
@@ -1710,7 +1747,7 @@ struct SegmentBackSink : NoCount {
 __global__ void __launch_bounds__(kKvSplitThreads, 2) kv_split_kernel(Params p) {
   using G = CtaGroup<kKvSplitThreads>;
   unsigned char* sm = smem_base();
-  const SmemLayout lay = smem_layout(EXACT_TOPK_FAMILY_KV_SPLIT, p.cap);
+  constexpr SmemLayout lay = smem_layout(EXACT_TOPK_FAMILY_KV_SPLIT, kKvSplitCap);
   Slot& sl = *reinterpret_cast<Slot*>(sm + lay.slots);
   GroupScratch& sc = *reinterpret_cast<GroupScratch*>(sm + lay.scratch);
   uint32_t* hist = reinterpret_cast<uint32_t*>(sm + lay.hist);
