@@ -200,18 +200,26 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
 // the same bin become one shared atomic.  Rows of few distinct values
 // (constant rows, tie bands, signed zeros) would otherwise put every lane of a
 // warp on one shared address.
+// Shared-memory reduction add on a histogram that lives in this CTA's shared
+// memory, issued in the shared state space (the pointer may reach a function
+// as a generic address).
+__device__ __forceinline__ void smem_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.shared.add.u32 [%0], %1;" ::"r"((uint32_t)__cvta_generic_to_shared(p)), "r"(v)
+               : "memory");
+}
+
 struct RunHist {
   uint32_t bin = 0u, cnt = 0u;
   __device__ __forceinline__ void add(uint32_t* hist, uint32_t b) {
     if (cnt != 0u && b != bin) {
-      atomicAdd(&hist[bin], cnt);
+      smem_add(&hist[bin], cnt);
       cnt = 0u;
     }
     bin = b;
     ++cnt;
   }
   __device__ __forceinline__ void flush(uint32_t* hist) {
-    if (cnt != 0u) atomicAdd(&hist[bin], cnt);
+    if (cnt != 0u) smem_add(&hist[bin], cnt);
     cnt = 0u;
   }
 };
@@ -800,7 +808,7 @@ struct FrontierSink : NoCount {  // frontier entry + leading-digit histogram (eq
   uint32_t* hist;
   __device__ __forceinline__ void operator()(uint32_t p, int32_t i, uint32_t d) const {
     F.put(p, i, d);
-    atomicAdd(&hist[d >> 21], 1u);
+    smem_add(&hist[d >> 21], 1u);
   }
 };
 struct CommitSink : NoCount {  // committed straight to the output (E0 of eq. 20)
@@ -1386,7 +1394,7 @@ __device__ void sample_view(const Params& p, const float* row, int L, int a, uin
     }
 #pragma unroll
     for (int k = 0; k < 8; ++k)
-      if (t0 + k * G::kThreads + tid < nv) atomicAdd(&hist[coarse_bin(u[k])], 1u);
+      if (t0 + k * G::kThreads + tid < nv) smem_add(&hist[coarse_bin(u[k])], 1u);
   }
   G::sync();
   view_cutoffs<G>(p, hist, sc, sl);
