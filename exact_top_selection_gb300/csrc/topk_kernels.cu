@@ -32,10 +32,12 @@
 // evict-first hint, so the lines the Phase-1 view touched (loaded with normal
 // priority) tend to stay in L2 until the complete-row pass reaches them.
 
+#include <cuda.h>  // CUtensorMap and its encoder's types (the encoder is reached at run time)
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstring>
 #include <mutex>
 
 #include "etk_internal.h"
@@ -314,6 +316,14 @@ struct Params {
   int32_t* seg_counts;  // [M_cap][P][2]
   const int32_t* prev;
   int32_t* trace;
+  // Persistent kernel: tiled tensor map over the scores seen as
+  // [M_cap][N / s][s] (lines of s scores), whose column `a` of a row is that
+  // row's view; a box of {4, view_box, 1} carries view_box consecutive view
+  // entries (with the three scores that share their 16 bytes).  view_tma = 0:
+  // the view is gathered with plain loads.
+  int32_t view_tma;
+  int32_t view_box;
+  CUtensorMap view_map;
 };
 
 // Candidate frontier: logical entries [0, cap) live in shared memory, entries
@@ -353,6 +363,8 @@ constexpr int kQueueCap = 64;  // < 32 before a vector slot + at most 32 pushed 
 constexpr int kQueueWords = kQueueCap * 9;
 // Persistent kernel: warps [0, kRefineWarps) refine the row just classified
 // while the remaining warps claim the next row and run its Phase 1.
+// TMA view boxes of up to 256 view entries (4 KB each) per persistent CTA.
+constexpr uint32_t kViewBoxes = 4;
 #ifndef ETK_PREPARE_WARPS
 #define ETK_PREPARE_WARPS (kPersistentThreads / 128)
 #endif
@@ -367,6 +379,8 @@ struct SmemLayout {
   uint32_t hist;      // uint32[nslots][2048]
   uint32_t frontier;  // uint2[cap]
   uint32_t runs;      // KV-split run table, or 0
+  uint32_t vbuf;      // persistent: TMA view boxes, kViewBoxes x 4 KB (128-byte aligned), or 0
+  uint32_t vbar;      // persistent: the view copies' mbarrier, and its phase word, or 0
   uint32_t queues;    // uint32[warps][kQueueWords]
   uint32_t total;
 };
@@ -394,6 +408,15 @@ __host__ __device__ constexpr SmemLayout smem_layout(int family, int cap) {
   o = align16(o + (uint32_t)cap * 8u);
   l.runs = family == EXACT_TOPK_FAMILY_KV_SPLIT ? o : 0u;
   if (family == EXACT_TOPK_FAMILY_KV_SPLIT) o = align16(o + (3 * kMaxSplits + 1) * 4u);
+  l.vbuf = 0u;
+  l.vbar = 0u;
+  if (pers) {
+    o = (o + 127u) & ~127u;
+    l.vbuf = o;
+    o += kViewBoxes * 4096u;
+    l.vbar = o;
+    o = align16(o + 16u);
+  }
   l.queues = o;
   o = align16(o + qwarps * kQueueWords * 4u);
   l.total = o;
@@ -1477,6 +1500,69 @@ __device__ void exit_protocol(int32_t* counters) {
 }
 
 // ----------------------------------------------------------------------------
+// Shared-memory addresses, mbarriers and TMA copies
+// ----------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+// One TMA bulk copy global -> this CTA's shared memory, completing on `bar`.
+// Both addresses 16-byte aligned, bytes a positive multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0u;
+}
+// Bounded wait for phase 0 of `bar`; false when the limit ran out.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar) {
+  for (int it = 0; it < (1 << 20); ++it)
+    if (mbar_try_wait(bar, 0u)) return true;
+  return false;
+}
+
+// Bounded wait for phase `parity` of `bar`; false when the limit ran out.
+__device__ __forceinline__ bool mbar_wait_parity_bounded(uint32_t bar, uint32_t parity) {
+  for (int it = 0; it < (1 << 20); ++it)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+// One tiled TMA load of a 3-D box at (x, y, z) of `map` into this CTA's shared
+// memory at `dst` (16-byte aligned; x * 4 bytes a multiple of 16), completing
+// on `bar`.  The box's bytes must have been announced on `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+// ----------------------------------------------------------------------------
 // Kernel 1: persistent sampled
 // ----------------------------------------------------------------------------
 
@@ -1492,6 +1578,63 @@ __device__ void exit_protocol(int32_t* counters) {
 // into a second slot and histogram.  The next row's complete-row pass then
 // starts as soon as both groups are done.
 
+// The persistent CTA's TMA view buffer: kViewBoxes boxes of 4 KB, their
+// mbarrier and the barrier's phase word (bit 0: parity of the next phase;
+// bit 1: a copy timed out, the buffer is not used again).
+struct ViewDma {
+  uint32_t* buf;
+  uint32_t bar;
+  uint32_t* phase;
+};
+
+// Phase 1's view (eq. 13) by group G through the TMA engine.  Box q of
+// {4, box, 1} scores at (a & ~3, q * box, r) lands at buf + 1024 q, so view
+// entry t is buf[1024 (t / box) + 4 (t % box) + (a & 3)].  Entries past the
+// boxes (views longer than kViewBoxes boxes, or in the last partial line of a
+// row whose capacity N is not a multiple of s) are loaded directly, as are all
+// of them once a copy has timed out.  Entered with a cleared histogram; leaves
+// it dirty.
+template <class G>
+__device__ void sample_view_tma(const Params& p, int r, const float* row, int L, int a,
+                                uint32_t* hist, GroupScratch& sc, Slot& sl, const ViewDma& vd) {
+  const int nv = view_size(L, a, p.s);
+  const int tid = G::rank();
+  const int box = p.view_box;
+  const int lines = p.N / p.s;
+  const int covered = min(min(nv, lines), (int)kViewBoxes * box);
+  const int nq = (covered + box - 1) / box;
+  if (tid == 0) {
+    int ok = 0;
+    if ((*vd.phase & 2u) == 0u && nq > 0) {
+      // earlier generic reads of the buffer are ordered before the copies
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_expect_tx(vd.bar, (uint32_t)nq * (uint32_t)box * 16u);
+      for (int q = 0; q < nq; ++q)
+        tma_load_3d(smem_addr(vd.buf) + (uint32_t)q * 4096u, &p.view_map, a & ~3, q * box, r,
+                    vd.bar);
+      const uint32_t ph = *vd.phase & 1u;
+      if (mbar_wait_parity_bounded(vd.bar, ph)) {
+        *vd.phase = ph ^ 1u;
+        ok = 1;
+      } else {
+        *vd.phase = 2u;  // copies may still land: the buffer is retired
+        flag_status(p.counters, 4);
+      }
+    }
+    sc.bcast = ok;
+  }
+  G::sync();
+  const int lim = sc.bcast != 0 ? covered : 0;
+  for (int t = tid; t < nv; t += G::kThreads) {
+    const uint32_t u =
+        t < lim ? vd.buf[1024 * (t / box) + 4 * (t % box) + (a & 3)]
+                : __ldg(reinterpret_cast<const unsigned int*>(row) + a + (int64_t)t * p.s);
+    smem_add(&hist[coarse_bin(u)], 1u);
+  }
+  G::sync();
+  view_cutoffs<G>(p, hist, sc, sl);
+}
+
 // What Phase 1 left for a claimed row (Slot::route of the next-row slot).
 constexpr int kNextNone = -1;    // the queue is exhausted
 constexpr int kNextPad = 0;      // L <= K: padded output, no selection
@@ -1504,7 +1647,7 @@ constexpr int kNextGuess = 3;    // guess-source cutoff T0 in the slot
 // barrier.
 template <class V>
 __device__ void prepare_row(const Params& p, int M, int assigned, Slot& nx, uint32_t* vh,
-                            GroupScratch& sc) {
+                            GroupScratch& sc, const ViewDma& vd) {
   if (V::rank() == 0) {
     const int nr = assigned >= 0 ? assigned : (int)gridDim.x + atomicAdd(p.counters + kCtrQueue, 1);
     sc.bcast = nr;
@@ -1536,7 +1679,10 @@ __device__ void prepare_row(const Params& p, int M, int assigned, Slot& nx, uint
       if (view_size(L, a, p.s) >= (p.dual ? p.q1 : p.q0)) {
         clear_hist<V>(vh, 2048);
         V::sync();
-        sample_view<V>(p, row, L, a, vh, sc, nx);
+        if (p.view_tma)
+          sample_view_tma<V>(p, nr, row, L, a, vh, sc, nx, vd);
+        else
+          sample_view<V>(p, row, L, a, vh, sc, nx);
         kind = kNextSampled;
       } else {
         kind = kNextDirect;
@@ -1554,7 +1700,7 @@ __device__ void prepare_row(const Params& p, int M, int assigned, Slot& nx, uint
 // Entered and left at a CTA barrier.
 __device__ void persistent_row(const Params& p, int M, Slot& sl, Slot& nx, const Frontier& F,
                                uint32_t* hist, uint32_t* vhist, GroupScratch* sc2,
-                               uint32_t* queues) {
+                               uint32_t* queues, const ViewDma& vd) {
   using G = CtaGroup<kPersistentThreads>;
   using R = SubGroup<kRefineWarps * 32, 0, 1>;
   using V = SubGroup<kPersistentThreads - kRefineWarps * 32, kRefineWarps, 2>;
@@ -1642,7 +1788,7 @@ __device__ void persistent_row(const Params& p, int M, Slot& sl, Slot& nx, const
       finish_row<R>(p, sl, out_row);
       if (threadIdx.x == 0) write_slot_trace(p, sl);
     } else {
-      prepare_row<V>(p, M, -1, nx, vhist, sc2[1]);
+      prepare_row<V>(p, M, -1, nx, vhist, sc2[1], vd);
     }
   } else {
     if (kind != kNextPad) {
@@ -1651,13 +1797,13 @@ __device__ void persistent_row(const Params& p, int M, Slot& sl, Slot& nx, const
       finish_row<G>(p, sl, out_row);
       if (threadIdx.x == 0) write_slot_trace(p, sl);
     }
-    prepare_row<G>(p, M, -1, nx, vhist, sc2[1]);
+    prepare_row<G>(p, M, -1, nx, vhist, sc2[1], vd);
   }
   __syncthreads();
 }
 
 __global__ void __launch_bounds__(kPersistentThreads, 1024 / kPersistentThreads)
-    persistent_sampled_kernel(Params p) {
+    persistent_sampled_kernel(const __grid_constant__ Params p) {
   unsigned char* sm = smem_base();
   constexpr SmemLayout lay = smem_layout(EXACT_TOPK_FAMILY_PERSISTENT_SAMPLED, kPersistentCap);
   Slot* slots = reinterpret_cast<Slot*>(sm + lay.slots);  // [0] this row, [1] the next
@@ -1666,12 +1812,21 @@ __global__ void __launch_bounds__(kPersistentThreads, 1024 / kPersistentThreads)
   uint32_t* vhist = hist + kCoarseBins;
   uint32_t* queues = reinterpret_cast<uint32_t*>(sm + lay.queues);
   const Frontier F = make_frontier(p, reinterpret_cast<uint2*>(sm + lay.frontier), blockIdx.x);
+  const ViewDma vd{reinterpret_cast<uint32_t*>(sm + lay.vbuf), smem_addr(sm + lay.vbar),
+                   reinterpret_cast<uint32_t*>(sm + lay.vbar + 8)};
   const int M = live_rows(p);
   if ((int)blockIdx.x < M) {  // CTA-uniform
-    prepare_row<CtaGroup<kPersistentThreads>>(p, M, (int)blockIdx.x, slots[1], vhist, sc2[1]);
+    if (threadIdx.x == 0) {
+      mbar_init(vd.bar, 1u);
+      // the boxes' shared destination must be 128-byte aligned: otherwise the
+      // buffer is retired from the start and the view is gathered directly
+      *vd.phase = (smem_addr(vd.buf) & 127u) == 0u ? 0u : 2u;
+    }
+    __syncthreads();
+    prepare_row<CtaGroup<kPersistentThreads>>(p, M, (int)blockIdx.x, slots[1], vhist, sc2[1], vd);
     __syncthreads();
     while (slots[1].route != kNextNone)
-      persistent_row(p, M, slots[0], slots[1], F, hist, vhist, sc2, queues);
+      persistent_row(p, M, slots[0], slots[1], F, hist, vhist, sc2, queues, vd);
   }
   exit_protocol(p.counters);
 }
@@ -2034,9 +2189,6 @@ __host__ __device__ constexpr ClusterLayout cluster_layout() {
   return l;
 }
 
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -2074,40 +2226,6 @@ __device__ __forceinline__ uint32_t atom_add_peer(uint32_t a, uint32_t v) {
   asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(a), "r"(v) : "memory");
   return old;
 }
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-// One TMA bulk copy global -> this CTA's shared memory, completing on `bar`.
-// Both addresses 16-byte aligned, bytes a positive multiple of 16.
-__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                              uint32_t bar) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0u;
-}
-// Bounded wait for phase 0 of `bar`; false when the limit ran out.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar) {
-  for (int it = 0; it < (1 << 20); ++it)
-    if (mbar_try_wait(bar, 0u)) return true;
-  return false;
-}
-
 // Sums histogram `local` (nbins, a multiple of 4, at most 4 per thread) over
 // the P CTAs of the cluster into `sum`.  Group barrier before return.
 template <class G>
@@ -2680,6 +2798,49 @@ int set_attrs(KernelT kernel, int family, size_t smem) {
   return EXACT_TOPK_OK;
 }
 
+// cuTensorMapEncodeTiled, reached through the runtime's driver entry point
+// (no link-time dependency on the driver library); null when unavailable.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// The persistent kernel's view map (Params::view_map): the scores of row z as
+// lines of s, box {4, min(256, N / s), 1}.  Only when s and the row pitch are
+// multiples of 4 scores (16-byte strides, 16-byte x coordinates a & ~3) and
+// the base is 16-byte aligned; otherwise the kernel gathers with plain loads.
+bool encode_view_map(Params& p) {
+  if (p.s < 4 || (p.s & 3) != 0 || (p.pitch & 3) != 0 || p.N < p.s || p.M_cap < 1) return false;
+  if ((reinterpret_cast<uintptr_t>(p.logits) & 15u) != 0u) return false;
+  const EncodeTiledFn fn = encode_tiled();
+  if (fn == nullptr) return false;
+  const cuuint64_t lines = (cuuint64_t)(p.N / p.s);
+  const cuuint32_t box = (cuuint32_t)(lines < 256u ? lines : 256u);
+  const cuuint64_t dims[3] = {(cuuint64_t)p.s, lines, (cuuint64_t)p.M_cap};
+  const cuuint64_t strides[2] = {(cuuint64_t)p.s * 4u, (cuuint64_t)p.pitch * 4u};
+  const cuuint32_t boxdim[3] = {4u, box, 1u};
+  const cuuint32_t estride[3] = {1u, 1u, 1u};
+  if (fn(&p.view_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3u, const_cast<float*>(p.logits), dims,
+         strides, boxdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  p.view_box = (int32_t)box;
+  return true;
+}
+
 }  // namespace
 
 size_t shared_bytes(int family, int cap) {
@@ -2694,6 +2855,7 @@ int kernel_occupancy(int family, int device, int* ctas_per_sm) {
   int rc = EXACT_TOPK_OK, n = 0;
   cudaError_t e = cudaSuccess;
   if (family == EXACT_TOPK_FAMILY_PERSISTENT_SAMPLED) {
+    (void)encode_tiled();  // resolved here, at planning time, not inside a capture
     const size_t smem = shared_bytes(family, kPersistentCap);
     rc = set_attrs(persistent_sampled_kernel, EXACT_TOPK_FAMILY_PERSISTENT_SAMPLED, smem);
     if (rc == EXACT_TOPK_OK)
@@ -2753,6 +2915,10 @@ int launch(const exact_topk_plan& plan, const LaunchArgs& a, cudaStream_t stream
                      : nullptr;
   p.prev = a.prev_topk;
   p.trace = a.trace;
+  p.view_tma = 0;
+  p.view_box = 0;
+  memset(&p.view_map, 0, sizeof(p.view_map));
+  if (plan.family == EXACT_TOPK_FAMILY_PERSISTENT_SAMPLED && encode_view_map(p)) p.view_tma = 1;
   const size_t smem = shared_bytes(plan.family, plan.cand_capacity);
   int rc = EXACT_TOPK_OK;
   switch (plan.family) {
