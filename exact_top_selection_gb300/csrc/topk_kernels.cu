@@ -1587,63 +1587,44 @@ struct ViewDma {
   uint32_t* phase;
 };
 
-// Leader only: starts the view boxes of row r, as many as its capacity N has
-// lines (at most kViewBoxes), and returns their number; 0 when the buffer is
-// retired.  Box q of {4, box, 1} scores at (a & ~3, q * box, r) lands at
-// buf + 1024 q.  Only the row id is needed, so the copies start before the
-// row's length is known.
-__device__ int view_tma_issue(const Params& p, int r, const ViewDma& vd) {
-  if ((*vd.phase & 2u) != 0u) return 0;
-  const int a = view_phase(r, p.s, p.s_bits);
-  const int box = p.view_box;
-  const int lines = p.N / p.s;
-  const int covered = min(lines, (int)kViewBoxes * box);
-  const int nq = (covered + box - 1) / box;
-  if (nq <= 0) return 0;
-  // earlier generic reads of the buffer are ordered before the copies
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  mbar_expect_tx(vd.bar, (uint32_t)nq * (uint32_t)box * 16u);
-  for (int q = 0; q < nq; ++q)
-    tma_load_3d(smem_addr(vd.buf) + (uint32_t)q * 4096u, &p.view_map, a & ~3, q * box, r, vd.bar);
-  return nq;
-}
-
-// Leader only: waits for the boxes started by view_tma_issue; false, with the
-// buffer retired (copies may still land in it) and the status flagged, when
-// the bounded wait runs out.
-__device__ bool view_tma_wait(const Params& p, const ViewDma& vd) {
-  const uint32_t ph = *vd.phase & 1u;
-  if (mbar_wait_parity_bounded(vd.bar, ph)) {
-    *vd.phase = ph ^ 1u;
-    return true;
-  }
-  *vd.phase = 2u;
-  flag_status(p.counters, 4);
-  return false;
-}
-
-// Phase 1's view (eq. 13) by group G from the TMA boxes: view entry t is
-// buf[1024 (t / box) + 4 (t % box) + (a & 3)].  `issued` (leader only) is the
-// number of boxes already started for this row, or -1 to start them here.
-// Entries past the boxes (views longer than kViewBoxes boxes, or in the last
-// partial line of a row whose capacity N is not a multiple of s) are loaded
-// directly, as are all of them once a copy has timed out.  Entered with a
-// cleared histogram; leaves it dirty.
+// Phase 1's view (eq. 13) by group G through the TMA engine.  Box q of
+// {4, box, 1} scores at (a & ~3, q * box, r) lands at buf + 1024 q, so view
+// entry t is buf[1024 (t / box) + 4 (t % box) + (a & 3)].  Entries past the
+// boxes (views longer than kViewBoxes boxes, or in the last partial line of a
+// row whose capacity N is not a multiple of s) are loaded directly, as are all
+// of them once a copy has timed out.  Entered with a cleared histogram; leaves
+// it dirty.
 template <class G>
 __device__ void sample_view_tma(const Params& p, int r, const float* row, int L, int a,
-                                uint32_t* hist, GroupScratch& sc, Slot& sl, const ViewDma& vd,
-                                int issued) {
+                                uint32_t* hist, GroupScratch& sc, Slot& sl, const ViewDma& vd) {
   const int nv = view_size(L, a, p.s);
   const int tid = G::rank();
   const int box = p.view_box;
   const int lines = p.N / p.s;
-  const int covered = min(lines, (int)kViewBoxes * box);
+  const int covered = min(min(nv, lines), (int)kViewBoxes * box);
+  const int nq = (covered + box - 1) / box;
   if (tid == 0) {
-    const int nq = issued >= 0 ? issued : view_tma_issue(p, r, vd);
-    sc.bcast = nq > 0 && view_tma_wait(p, vd) ? 1 : 0;
+    int ok = 0;
+    if ((*vd.phase & 2u) == 0u && nq > 0) {
+      // earlier generic reads of the buffer are ordered before the copies
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_expect_tx(vd.bar, (uint32_t)nq * (uint32_t)box * 16u);
+      for (int q = 0; q < nq; ++q)
+        tma_load_3d(smem_addr(vd.buf) + (uint32_t)q * 4096u, &p.view_map, a & ~3, q * box, r,
+                    vd.bar);
+      const uint32_t ph = *vd.phase & 1u;
+      if (mbar_wait_parity_bounded(vd.bar, ph)) {
+        *vd.phase = ph ^ 1u;
+        ok = 1;
+      } else {
+        *vd.phase = 2u;  // copies may still land: the buffer is retired
+        flag_status(p.counters, 4);
+      }
+    }
+    sc.bcast = ok;
   }
   G::sync();
-  const int lim = sc.bcast != 0 ? min(nv, covered) : 0;
+  const int lim = sc.bcast != 0 ? covered : 0;
   for (int t = tid; t < nv; t += G::kThreads) {
     const uint32_t u =
         t < lim ? vd.buf[1024 * (t / box) + 4 * (t % box) + (a & 3)]
@@ -1667,10 +1648,8 @@ constexpr int kNextGuess = 3;    // guess-source cutoff T0 in the slot
 template <class V>
 __device__ void prepare_row(const Params& p, int M, int assigned, Slot& nx, uint32_t* vh,
                             GroupScratch& sc, const ViewDma& vd) {
-  int issued = -1;  // leader: view boxes started for the claimed row, or -1
   if (V::rank() == 0) {
     const int nr = assigned >= 0 ? assigned : (int)gridDim.x + atomicAdd(p.counters + kCtrQueue, 1);
-    if (nr < M && p.view_tma && p.prev == nullptr) issued = view_tma_issue(p, nr, vd);
     sc.bcast = nr;
     sc.bcast2 = nr < M ? row_length(p, nr) : 0;
   }
@@ -1700,10 +1679,9 @@ __device__ void prepare_row(const Params& p, int M, int assigned, Slot& nx, uint
       if (view_size(L, a, p.s) >= (p.dual ? p.q1 : p.q0)) {
         clear_hist<V>(vh, 2048);
         V::sync();
-        if (p.view_tma) {
-          sample_view_tma<V>(p, nr, row, L, a, vh, sc, nx, vd, issued);
-          issued = -1;  // waited for inside
-        } else
+        if (p.view_tma)
+          sample_view_tma<V>(p, nr, row, L, a, vh, sc, nx, vd);
+        else
           sample_view<V>(p, row, L, a, vh, sc, nx);
         kind = kNextSampled;
       } else {
@@ -1712,9 +1690,6 @@ __device__ void prepare_row(const Params& p, int M, int assigned, Slot& nx, uint
     }
   }
   if (V::rank() == 0) {
-    // boxes started for a row that turned out to need no view are waited for,
-    // so that no copy is in flight when the buffer is next used
-    if (issued > 0) (void)view_tma_wait(p, vd);
     nx.row = nr;
     nx.L = L;
     nx.route = kind;
