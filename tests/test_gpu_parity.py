@@ -277,6 +277,31 @@ def test_worker_count_does_not_change_values():
     assert all(np.array_equal(traces[0], t) for t in traces[1:])
 
 
+def test_persistent_long_views_and_mixed_rows():
+    # Views longer than the TMA boxes cover (N / s = 3125 lines: the first
+    # 1024 entries from the boxes, the rest loaded directly), on few workers so
+    # that every CTA takes many rows through both tails (refinement beside the
+    # next row's Phase 1, and the whole-CTA tail of pad rows and spilled
+    # frontiers), with NaN garbage past ke that the boxes read but must not use.
+    M, N, K = 36, 100000, 2048
+    rng = np.random.default_rng(2026)
+    X = rng.standard_normal((M, N)).astype(np.float32)
+    ke = rng.integers(K + 1, N + 1, M).astype(np.int32)
+    ke[3], ke[11], ke[20] = 0, K, 5
+    X[7] = 1.25                                  # constant: |Q0| = L, spilled
+    X[15] = (np.arange(N) % 3).astype(np.float32)  # three-level ties
+    ke[7], ke[15], ke[30] = N, N, N
+    for r in range(M):
+        X[r, ke[r]:] = np.nan
+    for workers in (3, 0):
+        out, tr, plan, ctr = run_gpu(X, ke, K, family=etk.FAMILY_PERSISTENT_SAMPLED, stride=32,
+                                     workers=workers)
+        compare_rows(X, ke, K, out)
+        assert_counters_zero(ctr)
+        _, tr_ref = oracle_trace_for_plan(X, ke, K, plan)
+        compare_trace(tr, tr_ref)
+
+
 def test_default_entry_point_matches_plan_entry_point():
     # exact_topk (default plan, PR-style API) vs the oracle, through the
     # workspace_size / topk pair exactly as the pages' API describes.
