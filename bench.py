@@ -426,11 +426,13 @@ def _route_stats(trace, K):
 
 
 def run_sweep(args):
-    """Planner studies on one GPU: one JSON line per
-    point.  crossover: row width N against the row-local exact kernel and the
-    two sampled policies; margins: retention margin rho and view stride s on
-    prefill-shaped rows, with route rates; splits: KV-split segment count P on
-    the few-long-rows workload."""
+    """Planner studies on one GPU: one JSON line per point.  crossover: row
+    width N against the row-local exact kernel and the two sampled policies;
+    margins: retention margin rho and view stride s on prefill-shaped rows,
+    with route rates; splits: KV-split segment count P on the few-long-rows
+    workload; trace: a serving-style sequence of calls with N growing and
+    M = 2^24 / N, each planned by the default planner, timed call by call and
+    as one captured sequence."""
     import math
 
     import torch
@@ -490,6 +492,48 @@ def run_sweep(args):
                 emit({"sweep": "margins", "M": M, "N": N, "K": K, "stride": s,
                       "rho0": rho[0] / rho[1], "rho1": rho1[0] / rho1[1],
                       "us_per_call": sec * 1e6, "gbs": alg / sec / 1e9, **_route_stats(tr, K)})
+    elif args.sweep == "trace":
+        calls = workloads.trace_sequence(1 << 24, K, 20260020, device=str(device))
+        torch.cuda.synchronize(device)
+        runners, outs, total_rows, total_alg = [], [], 0, 0
+        for i, (X, ke) in enumerate(calls):
+            M, N = X.shape
+            runner = etk.ExactTopK(M, N, K, device=device)
+            tr = torch.full((M, 8), -9, dtype=torch.int32, device=device)
+            sec = _time_calls(runner, copies_for(X), ke, stream, trace=tr)
+            alg = int(ke.to(torch.int64).clamp(0, N).sum().item()) * 4 + M * K * 4
+            total_rows += M
+            total_alg += alg
+            runners.append(runner)
+            outs.append(torch.empty(M, K, dtype=torch.int32, device=device))
+            emit({"sweep": "trace", "call": i, "M": M, "N": N, "K": K,
+                  "family": etk.FAMILY_NAMES[runner.plan.family], "splits": runner.plan.splits,
+                  "us_per_call": sec * 1e6, "gbs": alg / sec / 1e9, **_route_stats(tr, K)})
+        # the whole sequence as one graph, replayed
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            for (X, ke), runner, out in zip(calls, runners, outs):
+                runner(X, ke, out=out, stream=stream)
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for (X, ke), runner, out in zip(calls, runners, outs):
+                    runner(X, ke, out=out, stream=stream)
+        g.replay()
+        torch.cuda.synchronize(device)
+        times = []
+        for _ in range(7):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+            torch.cuda.synchronize(device)
+            times.append(e0.elapsed_time(e1) / 1e3)
+        sec = sorted(times)[len(times) // 2]
+        emit({"sweep": "trace_sequence", "calls": len(calls), "rows": total_rows,
+              "us_per_sequence": sec * 1e6, "rows_per_s": total_rows / sec,
+              "gbs": total_alg / sec / 1e9})
     elif args.sweep == "splits":
         X, ke, _ = workloads.generate("long_decode", device=str(device))
         M, N = X.shape
@@ -731,7 +775,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-seconds", type=float, default=60.0)
-    ap.add_argument("--sweep", choices=["crossover", "margins", "splits"], default=None,
+    ap.add_argument("--sweep", choices=["crossover", "margins", "splits", "trace"], default=None,
                     help="planner study instead of the bench line (one JSON line per point)")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -150,22 +150,34 @@ int exact_topk_make_plan(int64_t num_rows, int64_t max_kv_len, int64_t row_pitch
   p.top_k = top_k;
   p.sm_count = info->sm_count;
 
-  // Family (section 5.5, Fig. 6): row-local exact below the sampling
-  // crossover (section 6.4 places it between 16-24K and 64K columns on H20;
-  // on GB300 the sampled path already wins at 16K, K = 2048); when rows
-  // cannot fill the device, the cluster split if a
-  // row fits the shared memory of one cluster (and its CTAs fit in about
-  // two waves), else the KV-split; persistent sampled otherwise.
+  // Family (section 5.5, Fig. 6).
+  // - Rows narrower than 16K: row-local exact below the sampling crossover
+  //   (section 6.4 places it between 16-24K and 64K columns on H20).  On
+  //   GB300 the sampled path wins from 4K columns (K = 2048) once the rows
+  //   need more than one wave of row-local CTAs, so the exact kernel keeps
+  //   only single-wave batches and rows under 4K.
+  // - Fewer rows than SMs: the cluster split if a row fits the shared memory
+  //   of one cluster (and its CTAs fit in about two waves), else the KV-split,
+  //   unless the KV-split would give each row a single segment: the
+  //   persistent kernel then runs the same one-CTA-per-row work faster.
+  // - Persistent sampled otherwise.
   const int64_t cluster_P = ceil_div64(max_kv_len, kClusterStage);
+  const int64_t rowlocal_wave =
+      (int64_t)info->sm_count * (info->rowlocal_ctas_per_sm > 0 ? info->rowlocal_ctas_per_sm : 1);
+  const int64_t kv_target =
+      (int64_t)info->sm_count * (info->kvsplit_ctas_per_sm > 0 ? info->kvsplit_ctas_per_sm : 1) / 4;
   int family = r.family;
   if (family == EXACT_TOPK_FAMILY_AUTO) {
     if (max_kv_len < 16384)
-      family = EXACT_TOPK_FAMILY_ROW_LOCAL_EXACT;
+      family = (max_kv_len >= 4096 && num_rows > rowlocal_wave)
+                   ? EXACT_TOPK_FAMILY_PERSISTENT_SAMPLED
+                   : EXACT_TOPK_FAMILY_ROW_LOCAL_EXACT;
     else if (num_rows < info->sm_count)
       family = (cluster_P <= kClusterMaxSplits && info->cluster_ctas_per_sm > 0 &&
                 num_rows * cluster_P <= 2LL * info->sm_count * info->cluster_ctas_per_sm)
                    ? EXACT_TOPK_FAMILY_CLUSTER_SPLIT
-                   : EXACT_TOPK_FAMILY_KV_SPLIT;
+                   : (num_rows >= kv_target ? EXACT_TOPK_FAMILY_PERSISTENT_SAMPLED
+                                            : EXACT_TOPK_FAMILY_KV_SPLIT);
     else
       family = EXACT_TOPK_FAMILY_PERSISTENT_SAMPLED;
   }
@@ -225,7 +237,7 @@ int exact_topk_make_plan(int64_t num_rows, int64_t max_kv_len, int64_t row_pitch
     // span; on GB300 the few-long-rows workload is fastest at this P).
     int64_t P = r.splits;
     if (P == 0) {
-      const int64_t target = (int64_t)info->sm_count * ctas_per_sm / 4;
+      const int64_t target = kv_target;
       P = 1;
       while (P < 64 && num_rows * P < target) P *= 2;
       while (P > 1 && max_kv_len / P < 8192) P /= 2;

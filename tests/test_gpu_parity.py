@@ -302,6 +302,22 @@ def test_persistent_long_views_and_mixed_rows():
         compare_trace(tr, tr_ref)
 
 
+def test_trace_sequence_default_planner():
+    # A serving-style sequence (N growing, M = 2^22 / N, ragged lengths, NaN
+    # tails) through the default planner: the calls land on all four kernel
+    # families and every row matches the oracle.
+    calls = workloads.trace_sequence(1 << 22, 2048, 314, device="cpu",
+                                     widths=(2048, 16384, 65536, 262144))
+    families = set()
+    for X, ke in calls:
+        out, tr, plan, ctr = run_gpu(X.numpy(), ke.numpy(), 2048)
+        families.add(plan.family)
+        compare_rows(X.numpy(), ke.numpy(), 2048, out)
+        assert_counters_zero(ctr)
+    assert families == {etk.FAMILY_ROW_LOCAL_EXACT, etk.FAMILY_PERSISTENT_SAMPLED,
+                        etk.FAMILY_CLUSTER_SPLIT, etk.FAMILY_KV_SPLIT}
+
+
 def test_default_entry_point_matches_plan_entry_point():
     # exact_topk (default plan, PR-style API) vs the oracle, through the
     # workspace_size / topk pair exactly as the pages' API describes.

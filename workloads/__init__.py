@@ -256,3 +256,25 @@ def decode_series(M, N, K, steps, seed, device="cpu", drift=0.05):
         Xt = X.clone()
         pad_with_nan(Xt, ke_t, g)
         yield Xt, ke_t
+
+
+TRACE_WIDTHS = (4096, 8192, 16384, 32768, 65536, 131072, 262144, 524288)
+
+
+def trace_sequence(total, K, seed, device="cpu", widths=TRACE_WIDTHS):
+    """A serving-style sequence of calls whose row width grows while the row
+    count shrinks with it (M = total // N, at least one row), the shape of an
+    engine moving from prefill chunks to long decode contexts.  Lengths are
+    uniform in [N/2, N] (at least one position), scores indexer-like with NaN
+    garbage beyond each length.
+
+    Returns a list of (X, ke) device tensors, one per call."""
+    g = _gen(device, seed)
+    calls = []
+    for N in widths:
+        M = max(1, total // N)
+        X = indexer_scores(M, N, g, device)
+        ke = _randint(g, max(1, N // 2), N, M, device).to(torch.int32)
+        pad_with_nan(X, ke, g)
+        calls.append((X, ke))
+    return calls
