@@ -153,9 +153,9 @@ int exact_topk_make_plan(int64_t num_rows, int64_t max_kv_len, int64_t row_pitch
   // Family (section 5.5, Fig. 6).
   // - Rows narrower than 16K: row-local exact below the sampling crossover
   //   (section 6.4 places it between 16-24K and 64K columns on H20).  On
-  //   GB300 the sampled path wins from 4K columns (K = 2048) once the rows
-  //   need more than one wave of row-local CTAs, so the exact kernel keeps
-  //   only single-wave batches and rows under 4K.
+  //   GB300 the sampled path wins from 1K columns (K from 64 to 2048) once
+  //   the rows need more than one wave of row-local CTAs, so the exact kernel
+  //   keeps only single-wave batches and rows under 1K columns (not measured).
   // - Fewer rows than SMs: the cluster split if a row fits the shared memory
   //   of one cluster (and its CTAs fit in about two waves), else the KV-split,
   //   unless the KV-split would give each row a single segment: the
@@ -169,7 +169,7 @@ int exact_topk_make_plan(int64_t num_rows, int64_t max_kv_len, int64_t row_pitch
   int family = r.family;
   if (family == EXACT_TOPK_FAMILY_AUTO) {
     if (max_kv_len < 16384)
-      family = (max_kv_len >= 4096 && num_rows > rowlocal_wave)
+      family = (max_kv_len >= 1024 && num_rows > rowlocal_wave)
                    ? EXACT_TOPK_FAMILY_PERSISTENT_SAMPLED
                    : EXACT_TOPK_FAMILY_ROW_LOCAL_EXACT;
     else if (num_rows < info->sm_count)

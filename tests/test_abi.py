@@ -48,9 +48,10 @@ def test_version_and_error_strings():
     (151, 131072, 2048, etk.FAMILY_PERSISTENT_SAMPLED, 128, 1),
     (128, 131072, 2048, etk.FAMILY_PERSISTENT_SAMPLED, 128, 1),
     (64, 262144, 2048, etk.FAMILY_KV_SPLIT, 128, 1),
-    # narrow rows: exact kernel for one wave of rows or rows under 4K columns
+    # narrow rows: exact kernel for one wave of rows or rows under 1K columns
     (100, 8192, 256, etk.FAMILY_ROW_LOCAL_EXACT, 64, 0),
-    (5000, 2048, 64, etk.FAMILY_ROW_LOCAL_EXACT, 64, 0),
+    (5000, 512, 64, etk.FAMILY_ROW_LOCAL_EXACT, 64, 0),
+    (5000, 2048, 64, etk.FAMILY_PERSISTENT_SAMPLED, 64, 0),
     (4096, 4096, 2048, etk.FAMILY_PERSISTENT_SAMPLED, 64, 0),
     (2048, 8192, 2048, etk.FAMILY_PERSISTENT_SAMPLED, 64, 0),
     (8, 140000, 2048, etk.FAMILY_KV_SPLIT, 128, 1),

@@ -304,15 +304,16 @@ def test_persistent_long_views_and_mixed_rows():
 
 def test_trace_sequence_default_planner():
     # A serving-style sequence (N growing, M = 2^22 / N, ragged lengths, NaN
-    # tails) through the default planner: the calls land on all four kernel
-    # families and every row matches the oracle.
+    # tails, K = min(2048, N / 4)) through the default planner: the calls land
+    # on all four kernel families and every row matches the oracle.
     calls = workloads.trace_sequence(1 << 22, 2048, 314, device="cpu",
-                                     widths=(2048, 16384, 65536, 262144))
+                                     widths=(512, 16384, 65536, 262144))
     families = set()
     for X, ke in calls:
-        out, tr, plan, ctr = run_gpu(X.numpy(), ke.numpy(), 2048)
+        K = min(2048, X.shape[1] // 4)
+        out, tr, plan, ctr = run_gpu(X.numpy(), ke.numpy(), K)
         families.add(plan.family)
-        compare_rows(X.numpy(), ke.numpy(), 2048, out)
+        compare_rows(X.numpy(), ke.numpy(), K, out)
         assert_counters_zero(ctr)
     assert families == {etk.FAMILY_ROW_LOCAL_EXACT, etk.FAMILY_PERSISTENT_SAMPLED,
                         etk.FAMILY_CLUSTER_SPLIT, etk.FAMILY_KV_SPLIT}
