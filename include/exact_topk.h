@@ -69,6 +69,13 @@ typedef enum exact_topk_status {
 #define EXACT_TOPK_MAX_N 0x7FFFFFF0LL    /* row width and pitch must fit int32 indices */
 
 typedef enum exact_topk_family {
+  /* The planner's choice, from the row count M, width N and the device:
+     - N < 16384: row-local exact when the rows fit one wave of its CTAs or
+       N < 1024, persistent sampled otherwise;
+     - M < SM count: cluster split when a row fits one cluster (N <= 8 * 16384)
+       and the clusters fit about two waves; otherwise the KV-split, unless it
+       would give each row a single segment (persistent sampled then);
+     - otherwise persistent sampled. */
   EXACT_TOPK_FAMILY_AUTO = 0,
   /* One CTA owns a row for all three phases; rows are claimed from a device
      queue in completion order (section 5.5, "Persistent sampled"). */
