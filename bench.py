@@ -1,9 +1,11 @@
 """Benchmark of exact row-wise FP32 Top-K on GB300.
 
 Metric: rows/s and score-row HBM GB/s (fraction of the measured GB300 HBM
-peak) per workload, 1 GPU.  The headline line is the decode batch (M=64,
-N=65536, ke ~ U[2048, 65536], K=2048, indexer-like scores); "per_config"
-repeats the measurement for all five workloads.
+peak) per workload, 1 GPU.  The headline line is the largest workload, the
+causal prefill batch (M=4096, N=131072, ke[r] = N - M + r + 1, K=2048,
+indexer-like scores with a positional trend); "per_config" repeats the
+measurement, with its own end-to-end and CPU-oracle numbers, for all five
+workloads.
 
 A step is one exact Top-K call (one kernel launch) over one batch whose
 inputs are already resident in HBM.  Inputs smaller than L2 are rotated over
@@ -37,7 +39,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-HEADLINE = "decode_batch"
+HEADLINE = "prefill_causal"
 MEASURED_PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
 PROFILES = os.path.join(ROOT, "profiles")
@@ -585,42 +587,98 @@ def e2e_measure(case, steps, warmup, stream):
     return dt, h2d, d2h
 
 
-def cpu_baseline(case_name, seconds=10.0, rows_cap=None):
-    """The oracle as it stands, on all host cores, over a bounded sample."""
+def cpu_baseline(case, seconds=10.0, rows_cap=None):
+    """The oracle as it stands, on all host cores, over a bounded sample: the
+    first `rows_cap` rows of the case's own (device-resident) matrix, copied
+    to the host, selected again and again until `seconds` have passed."""
     import numpy as np
 
     import oracle
-    import workloads
-    X, ke, K = workloads.generate(case_name, device="cpu")
-    X, ke = X.numpy(), ke.numpy()
-    M = X.shape[0] if rows_cap is None else min(rows_cap, X.shape[0])
+    M = case.M if rows_cap is None else max(1, min(rows_cap, case.M))
+    X = case.X[0][:M].cpu().numpy()
+    ke = case.ke[:M].cpu().numpy()
+    K = case.K
     threads = oracle.hardware_threads()
     rows = 0
     t0 = time.perf_counter()
     while True:
-        oracle.topk_rows(X[:M], ke[:M], K, nthreads=threads)
+        oracle.topk_rows(X, ke, K, nthreads=threads)
         rows += M
         if time.perf_counter() - t0 >= seconds:
             break
     dt = time.perf_counter() - t0
-    bytes_ = int(np.clip(ke[:M].astype(np.int64), 0, X.shape[1]).sum()) * 4 + M * K * 4
+    bytes_ = int(np.clip(ke.astype(np.int64), 0, X.shape[1]).sum()) * 4 + M * K * 4
     return {"value": rows / dt, "unit": "rows/s", "cores": threads, "kind": "oracle",
             "gbs": bytes_ * (rows / M) / dt / 1e9,
-            "sample": f"{case_name}: {M} of {X.shape[0]} rows per pass, {rows // M} passes "
+            "sample": f"{case.name}: rows 0..{M - 1} of {case.M}, {rows // M} passes "
                       f"in {dt:.1f} s (std::nth_element per row, {threads} threads)"}
+
+
+# rows of each workload the per-config CPU baseline selects per pass
+CPU_SAMPLE_ROWS = {"short_iid": 4, "decode_batch": 64, "prefill_causal": 256, "long_decode": 8,
+                   "adversarial": 256}
 
 
 # ---------------------------------------------------------------- arms
 
 
+def _e2e_entry(case, steps, warmup, stream):
+    dt, h2d, d2h = e2e_measure(case, steps, warmup, stream)
+    e_dt, e_rows = aggregate_over_ranks(dt, case.M * steps)
+    return {"value": e_rows / e_dt, "unit": "rows/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": dt / steps * 1e3,
+            "path": "pinned host -> H2D -> exact_topk_run (C ABI) -> D2H, per step"}
+
+
+def init_ranks(args):
+    """Process group of a replica run (one process per GPU, rows split by
+    rank, no collective on the data path; the group only carries the
+    whole-job time and row totals).  Returns (rank, local_rank, world)."""
+    rank, local_rank, world = dist_env()
+    if world != args.gpus:
+        raise SystemExit(f"bench.py: --gpus {args.gpus} disagrees with WORLD_SIZE={world}")
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if (torch.cuda.is_available() and not args.stub) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local_rank)
+        dist.init_process_group(backend)
+    return rank, local_rank, world
+
+
+def finish_ranks(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_stub(args):
+    """The launcher and the whole-job aggregation without a GPU: every rank
+    'times' a fixed sleep over a fixed row count.  Used by the CPU tests of
+    the replica launcher; its line says "stub" and is not a measurement."""
+    rank, _, world = init_ranks(args)
+    rows = 64
+    barrier()
+    t0 = time.perf_counter()
+    time.sleep(0.02 * (rank + 1))
+    elapsed = time.perf_counter() - t0
+    barrier()
+    e_max, rows_total = aggregate_over_ranks(elapsed, rows * args.steps)
+    if rank == 0:
+        print(json.dumps({"stub": True, "metric": "rows/s (launcher test, no GPU)",
+                          "value": rows_total / e_max, "unit": "rows/s", "n_gpus": world,
+                          "steps": args.steps, "warmup": args.warmup,
+                          "ms_per_step": e_max / args.steps * 1e3, "higher_is_better": True,
+                          "scaling": "weak", "rows_total": rows_total,
+                          "max_rank_seconds": e_max}), flush=True)
+    finish_ranks(world)
+
+
 def run_ours(args):
     import torch
 
-    rank, local_rank, world = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local_rank)
-        dist.init_process_group("nccl")
+    rank, local_rank, world = init_ranks(args)
     device = torch.device("cuda", local_rank if world > 1 else torch.cuda.current_device())
     torch.cuda.set_device(device)
     stream = torch.cuda.Stream(device)
@@ -641,25 +699,19 @@ def run_ours(args):
     achieved = case.alg_bytes / per_call / 1e9
     kernel = KERNEL_NAMES[case.plan.family]
     traffic = profiled_traffic(kernel, case.name)
+    e2e_steps = max(3, min(args.steps, 200))
+    e2e = None if args.no_e2e else _e2e_entry(case, e2e_steps, args.warmup, stream)
 
-    e2e = None
-    if not args.no_e2e:
-        dt, h2d, d2h = e2e_measure(case, max(3, min(args.steps, 200)), args.warmup, stream)
-        n_e2e = max(3, min(args.steps, 200))
-        e_dt, e_rows = aggregate_over_ranks(dt, case.M * n_e2e)
-        e2e = {"value": e_rows / e_dt, "unit": "rows/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": dt / n_e2e * 1e3,
-               "path": "pinned host -> H2D -> exact_topk_run (C ABI) -> D2H, per step"}
-
+    # Per-workload table (one process only: a replica run times the headline).
     per_config = {}
-    if args.all_configs:
+    if args.all_configs and world == 1:
         import workloads
         for name in workloads.ORDER:
             c = case if (name == case.name and args.rows is None) else \
                 Case(name, device, seed_offset=rank)
             sec = median_per_call(c, stream)
             gbs = c.alg_bytes / sec / 1e9
-            per_config[name] = {
+            entry = {
                 "workload": c.w.description, "M": c.M, "N": c.N, "K": c.K,
                 "family": KERNEL_NAMES[c.plan.family], "stride": c.plan.stride,
                 "dual": c.plan.dual, "splits": c.plan.splits, "workers": c.plan.workers,
@@ -668,11 +720,21 @@ def run_ours(args):
                 "l2": c.l2_note(), "routes": c.route_rates(),
                 "traffic_bytes_per_launch": profiled_traffic(KERNEL_NAMES[c.plan.family], name),
             }
+            if c is case:
+                entry["e2e"] = e2e if e2e is not None else _e2e_entry(c, e2e_steps, args.warmup,
+                                                                      stream)
+            else:
+                entry["e2e"] = _e2e_entry(c, e2e_steps, args.warmup, stream)
+            if not args.no_cpu:
+                entry["cpu_baseline"] = (
+                    cpu_baseline(c, seconds=args.cpu_config_seconds,
+                                 rows_cap=CPU_SAMPLE_ROWS.get(name)))
+            per_config[name] = entry
             if c is not case:
                 del c
                 torch.cuda.empty_cache()
     guess_series = None
-    if args.all_configs:
+    if args.all_configs and world == 1:
         guess_series = guess_series_measure(device, stream)
         torch.cuda.empty_cache()
     sampler.stop()
@@ -680,7 +742,8 @@ def run_ours(args):
 
     cpu = None
     if world == 1 and not args.no_cpu:
-        cpu = cpu_baseline(case.name, seconds=args.cpu_seconds)
+        cpu = cpu_baseline(case, seconds=args.cpu_seconds,
+                           rows_cap=CPU_SAMPLE_ROWS.get(case.name))
 
     if rank == 0:
         line = {
@@ -708,10 +771,33 @@ def run_ours(args):
             "decode_guess_series": guess_series,
             "clocks_whole_run": clocks_all,
         }
-        print(json.dumps(line))
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
+        print(json.dumps(line), flush=True)
+    finish_ranks(world)
+
+
+def launch_replicas(args, argv):
+    """`bench.py --gpus N` started without a launcher: start N copies of this
+    script, one per GPU (RANK = LOCAL_RANK = i, WORLD_SIZE = N, rendezvous on
+    127.0.0.1), pass rank 0's JSON line through and fail if any rank fails."""
+    import socket
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    procs = []
+    for r in range(args.gpus):
+        env = dict(os.environ, RANK=str(r), LOCAL_RANK=str(r), WORLD_SIZE=str(args.gpus),
+                   MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+        procs.append(subprocess.Popen([sys.executable, os.path.abspath(__file__), *argv],
+                                      env=env, stdout=subprocess.PIPE if r == 0 else
+                                      subprocess.DEVNULL, text=True))
+    out, _ = procs[0].communicate()
+    rc = procs[0].returncode
+    for p in procs[1:]:
+        rc = max(rc, p.wait())
+    sys.stdout.write(out)
+    sys.stdout.flush()
+    return rc
 
 
 def run_reference(args):
@@ -724,8 +810,12 @@ def run_reference(args):
     rank, _, world = dist_env()
     if rank != 0:
         return
-    X, ke, K = workloads.generate(args.workload, device="cpu")
-    X, ke = X.numpy(), ke.numpy()
+    # The same matrix as our arm's rank 0 (made by the seeded generator on the
+    # GPU when there is one, which is only faster), selected on the host.
+    import torch
+    gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
+    X, ke, K = workloads.generate(args.workload, device=gen_dev)
+    X, ke = X.cpu().numpy(), ke.cpu().numpy()
     M, N = X.shape
     threads = oracle.hardware_threads()
     t0 = time.perf_counter()
@@ -774,6 +864,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-config-seconds", type=float, default=3.0,
+                    help="CPU-oracle sample length of each per-config entry")
+    ap.add_argument("--stub", action="store_true",
+                    help="launcher/aggregation test without a GPU (the line is not a measurement)")
     ap.add_argument("--reference-seconds", type=float, default=60.0)
     ap.add_argument("--sweep", choices=["crossover", "margins", "splits", "trace"], default=None,
                     help="planner study instead of the bench line (one JSON line per point)")
@@ -786,7 +880,14 @@ def parse_args(argv=None):
 
 
 def main(argv=None):
+    argv = sys.argv[1:] if argv is None else list(argv)
     args = parse_args(argv)
+    if args.gpus < 1:
+        raise SystemExit("bench.py: --gpus must be >= 1")
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        return launch_replicas(args, argv)
+    if args.stub:
+        return run_stub(args)
     if args.impl == "reference":
         run_reference(args)
     else:
@@ -799,4 +900,4 @@ def main(argv=None):
 
 
 if __name__ == "__main__":
-    main()
+    sys.exit(main() or 0)

@@ -66,6 +66,13 @@ struct WorkspaceLayout {
 };
 WorkspaceLayout workspace_layout(const exact_topk_plan& plan);
 
+// Every host-side check of exact_topk_run (pointers, shapes, plan
+// consistency, buffer sizes, alignment); EXACT_TOPK_OK or the error status.
+int check_run(const exact_topk_plan* plan, const float* logits, const int32_t* ke,
+              const int32_t* out, const int32_t* num_valid_rows, const void* counters,
+              size_t counter_bytes, const void* workspace, size_t workspace_bytes,
+              const int32_t* prev_topk, const int32_t* trace);
+
 // Implemented in topk_kernels.cu.
 int kernel_occupancy(int family, int device, int* ctas_per_sm);
 int launch(const exact_topk_plan& plan, const LaunchArgs& args, cudaStream_t stream);

@@ -25,6 +25,8 @@ int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 bool is_pow2(int64_t v) { return v > 0 && (v & (v - 1)) == 0; }
 
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
 // Per-device cache of exact_topk_device_info (the attribute queries and the
 // kernel attribute setup run once per device, before any capture).
 constexpr int kMaxDevices = 64;
@@ -279,12 +281,14 @@ int exact_topk_workspace_size(int64_t num_rows, int64_t max_kv_len, int top_k,
   return EXACT_TOPK_OK;
 }
 
-static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+}  // extern "C"
 
-int exact_topk_run(const exact_topk_plan* plan, const float* logits, const int32_t* ke,
-                   int32_t* out, const int32_t* num_valid_rows, void* counters,
-                   size_t counter_bytes, void* workspace, size_t workspace_bytes,
-                   const int32_t* prev_topk, int32_t* trace, struct CUstream_st* stream) {
+namespace etk {
+
+int check_run(const exact_topk_plan* plan, const float* logits, const int32_t* ke,
+              const int32_t* out, const int32_t* num_valid_rows, const void* counters,
+              size_t counter_bytes, const void* workspace, size_t workspace_bytes,
+              const int32_t* prev_topk, const int32_t* trace) {
   if (plan == nullptr || logits == nullptr || ke == nullptr || out == nullptr ||
       counters == nullptr)
     return EXACT_TOPK_ERR_NULL_POINTER;
@@ -324,6 +328,20 @@ int exact_topk_run(const exact_topk_plan* plan, const float* logits, const int32
       (num_valid_rows != nullptr && !aligned(num_valid_rows, 4)) ||
       (prev_topk != nullptr && !aligned(prev_topk, 4)) || (trace != nullptr && !aligned(trace, 4)))
     return EXACT_TOPK_ERR_MISALIGNED;
+  return EXACT_TOPK_OK;
+}
+
+}  // namespace etk
+
+extern "C" {
+
+int exact_topk_run(const exact_topk_plan* plan, const float* logits, const int32_t* ke,
+                   int32_t* out, const int32_t* num_valid_rows, void* counters,
+                   size_t counter_bytes, void* workspace, size_t workspace_bytes,
+                   const int32_t* prev_topk, int32_t* trace, struct CUstream_st* stream) {
+  const int rc = check_run(plan, logits, ke, out, num_valid_rows, counters, counter_bytes,
+                           workspace, workspace_bytes, prev_topk, trace);
+  if (rc != EXACT_TOPK_OK) return rc;
   LaunchArgs a;
   a.logits = logits;
   a.ke = ke;

@@ -2975,12 +2975,11 @@ int launch(const exact_topk_plan& plan, const LaunchArgs& a, cudaStream_t stream
 // ----------------------------------------------------------------------------
 //
 // Some callers cannot allocate device memory at the point where they need a
-// Top-K: code that runs while a stream capture is already open (a cudaMalloc
-// there would invalidate the capture), plugins whose host framework owns every
-// device allocation, and latency-critical loops where cudaMalloc's implicit
-// device synchronization is unacceptable.  For them this entry point runs the
-// KV-split kernel with its counters and workspace carved out of one file-scope
-// device array instead of caller-provided buffers.
+// Top-K: plugins whose host framework owns every device allocation, and
+// latency-critical loops where cudaMalloc's implicit device synchronization is
+// unacceptable.  For them this entry point runs the KV-split kernel with its
+// counters and workspace carved out of one file-scope device array instead of
+// caller-provided buffers.
 
 namespace etk {
 namespace {
@@ -3043,6 +3042,11 @@ extern "C" int exact_topk_kv_split_noalloc(const float* logits, int64_t num_rows
   if (ctr_bytes + plan.workspace_bytes > kNoAllocScratchBytes)
     return EXACT_TOPK_ERR_WORKSPACE_TOO_SMALL;
   unsigned char* scratch = static_cast<unsigned char*>(base);
+  // Every argument check runs before anything is enqueued, so a rejected call
+  // leaves the stream and the array untouched.
+  rc = check_run(&plan, logits, ke, out, num_valid_rows, scratch, (size_t)plan.counter_bytes,
+                 scratch + ctr_bytes, (size_t)plan.workspace_bytes, nullptr, nullptr);
+  if (rc != EXACT_TOPK_OK) return rc;
   // The array keeps whatever the previous call left; the counters must start
   // at zero, so clear them on the stream (a memset, not an allocation).
   if (cudaMemsetAsync(scratch, 0, (size_t)plan.counter_bytes,

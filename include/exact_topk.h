@@ -207,12 +207,12 @@ int exact_topk_run(const exact_topk_plan* plan, const float* logits, const int32
                    size_t counter_bytes, void* workspace, size_t workspace_bytes,
                    const int32_t* prev_topk, int32_t* trace, struct CUstream_st* stream);
 
-/* Allocation-free variant of exact_topk for callers that cannot allocate
- * device memory where they need the selection: code running while a stream
- * capture is already open (a cudaMalloc there would invalidate the capture),
- * plugins whose host framework owns every device allocation, and
- * latency-critical loops where cudaMalloc's implicit device synchronization is
- * not acceptable.  The paper has no counterpart to this entry point.
+/* Allocation-free variant of exact_topk, for callers that cannot allocate
+ * device memory where they need the selection: plugins and extensions whose
+ * host framework owns every device allocation (and hands them only the
+ * tensors of the operation), and latency-critical loops where cudaMalloc's
+ * implicit device synchronization is not acceptable.  The paper has no
+ * counterpart to this entry point.
  *
  * It always runs the KV-split kernel family (planned as for exact_topk with
  * the family fixed) and takes its counters and workspace from one static
@@ -222,7 +222,8 @@ int exact_topk_run(const exact_topk_plan* plan, const float* logits, const int32
  * rules of exact_topk; there is no guess source.
  *   - Shapes whose KV-split counters (rounded up to 256 bytes) plus workspace
  *     (about num_rows * max_kv_len * 8 bytes) exceed the array are rejected
- *     with EXACT_TOPK_ERR_WORKSPACE_TOO_SMALL; nothing is launched.
+ *     with EXACT_TOPK_ERR_WORKSPACE_TOO_SMALL.  Every argument is checked
+ *     before anything is enqueued: a rejected call launches nothing.
  *   - The first call on a device sets up (the array's device address, device
  *     attributes, kernel attributes): make it before any stream capture.
  *   - Each call enqueues a memset of the counter region and one kernel on
@@ -230,6 +231,9 @@ int exact_topk_run(const exact_topk_plan* plan, const float* logits, const int32
  *   - Every call on a device shares the one array, which keeps the previous
  *     call's contents: calls that overlap on the GPU (other streams, other
  *     host threads) race and must be serialized by the caller.
+ *   - The sticky device-side status word (set when an internal consistency
+ *     guard trips, which valid inputs never do) lives in that array and is
+ *     cleared by the next call: this entry point cannot report it.
  * Errors: as exact_topk. */
 #define EXACT_TOPK_NOALLOC_SCRATCH_BYTES (64u << 20)
 int exact_topk_kv_split_noalloc(const float* logits, int64_t num_rows, int64_t max_kv_len,

@@ -51,3 +51,38 @@ def test_aggregate_over_two_gloo_ranks():
 def test_single_process_aggregate_is_identity():
     import bench
     assert bench.aggregate_over_ranks(0.5, 64) == (0.5, 64)
+
+
+def _bench(args, env=None):
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    e = {k: v for k, v in os.environ.items()
+         if k not in ("RANK", "LOCAL_RANK", "WORLD_SIZE", "MASTER_ADDR", "MASTER_PORT")}
+    e.update(env or {})
+    res = subprocess.run([sys.executable, os.path.join(root, "bench.py"), *args], env=e,
+                         capture_output=True, text=True, timeout=240)
+    lines = [json.loads(x) for x in res.stdout.splitlines() if x.startswith("{")]
+    return res.returncode, lines, res.stderr
+
+
+def test_bench_gpus_two_starts_two_replica_ranks():
+    """`bench.py --gpus 2` without a launcher starts two ranks itself (gloo
+    here, the stub arm standing in for the timed GPU region) and prints one
+    line whose totals cover both ranks."""
+    rc, lines, err = _bench(["--gpus", "2", "--stub", "--steps", "5", "--warmup", "3"])
+    assert rc == 0, err
+    assert len(lines) == 1, lines
+    line = lines[0]
+    assert line["stub"] is True and line["n_gpus"] == 2 and line["scaling"] == "weak"
+    assert line["rows_total"] == 2 * 64 * 5
+    # the slowest rank (rank 1 sleeps 40 ms) sets the whole-job time
+    assert line["max_rank_seconds"] >= 0.04
+    assert abs(line["value"] - line["rows_total"] / line["max_rank_seconds"]) < 1e-6 * line["value"]
+
+
+def test_bench_refuses_gpus_that_disagree_with_world_size():
+    rc, lines, _ = _bench(["--gpus", "2", "--stub", "--steps", "1", "--warmup", "3"],
+                          env={"WORLD_SIZE": "1", "RANK": "0", "LOCAL_RANK": "0"})
+    assert rc != 0 and not lines
