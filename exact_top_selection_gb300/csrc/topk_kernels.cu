@@ -365,8 +365,11 @@ constexpr int kQueueWords = kQueueCap * 9;
 // while the remaining warps claim the next row and run its Phase 1.
 // TMA view boxes of up to 256 view entries (4 KB each) per persistent CTA.
 constexpr uint32_t kViewBoxes = 4;
+// Six of sixteen warps: with the range-relative refinement (refine_fast) the
+// next row's Phase 1 is the longer half of the tail; measured on the causal
+// prefill batch, 2, 4, 6 and 8 warps gave 470, 435, 429 and 433 us.
 #ifndef ETK_PREPARE_WARPS
-#define ETK_PREPARE_WARPS (kPersistentThreads / 128)
+#define ETK_PREPARE_WARPS (3 * kPersistentThreads / 256)
 #endif
 constexpr int kRefineWarps = kPersistentThreads / 32 - ETK_PREPARE_WARPS;
 static_assert(kRefineWarps > 0 && kRefineWarps < kPersistentThreads / 32,
@@ -1048,9 +1051,9 @@ __device__ uint32_t small_select(const uint32_t* v, uint32_t n, uint32_t vhi, ui
 // small_select: the same threshold, reached without further passes over the
 // global slice.
 template <class G>
-__device__ void refine(const Frontier& F, uint32_t n, uint32_t k, uint32_t* hist,
-                       GroupScratch& sc, Slot& sl, int32_t* out_row, int K, uint32_t* scratch,
-                       uint32_t scap) {
+__device__ void refine_digits(const Frontier& F, uint32_t n, uint32_t k, uint32_t* hist,
+                              GroupScratch& sc, Slot& sl, int32_t* out_row, int K,
+                              uint32_t* scratch, uint32_t scap) {
   const int tid = G::rank();
   const uint32_t lt = lanemask_lt();
   const uint32_t nr = (n + 31u) & ~31u;  // whole warps visit every slot index
@@ -1190,6 +1193,162 @@ __device__ void refine(const Frontier& F, uint32_t n, uint32_t k, uint32_t* hist
     }
   }
   G::sync();
+}
+
+// h0 of eq. 17 (leading 11-bit digit of every frontier key) rebuilt from a
+// frontier held in shared memory.
+template <class G>
+__device__ void rebuild_h0(const Frontier& F, uint32_t n, uint32_t* hist) {
+  G::sync();
+  clear_hist<G>(hist, 2048);
+  G::sync();
+  for (uint32_t p = G::rank(); p < n; p += G::kThreads) smem_add(&hist[F.s[p].y >> 21], 1u);
+  G::sync();
+}
+
+// Phase 3 for a frontier held in shared memory (n <= F.cap), reaching the
+// same threshold as eqs. 22-25 with digits taken over the frontier's own key
+// range [kmin, kmax] instead of fixed bit fields: frontier keys cluster in a
+// few leading-digit buckets, so a range-relative 11-bit digit usually leaves
+// a boundary bucket of a handful of keys after one histogram.  One pass then
+// commits every key below the boundary bucket and collects that bucket, whose
+// k' smallest keys are taken by one warp (32 keys or fewer) or by
+// small_select.  A frontier whose keys are all equal commits any k of them
+// (the tie fill of eq. 25).  Returns false, with nothing committed and h0
+// restored in `hist`, when the boundary bucket outgrows `scratch` (pcap
+// (key, index) pairs: keys at [0, pcap), indices at [pcap, 2 pcap)); the
+// caller then runs the fixed-digit recurrence.
+template <class G>
+__device__ bool refine_fast(const Frontier& F, uint32_t n, uint32_t k, uint32_t* hist,
+                            GroupScratch& sc, Slot& sl, int32_t* out_row, int K,
+                            uint32_t* scratch, uint32_t pcap) {
+  const int tid = G::rank();
+  const uint32_t lt = lanemask_lt();
+  const uint32_t nr = (n + 31u) & ~31u;
+  if (k == 0u || n < k) return k == 0u;  // n < k: inconsistent counts; finish_row flags it
+  uint32_t mn = 0xFFFFFFFFu, mx = 0u;
+  for (uint32_t p = tid; p < n; p += G::kThreads) {
+    const uint32_t d = F.s[p].y;
+    mn = min(mn, d);
+    mx = max(mx, d);
+  }
+  uint32_t kmin, kmax;
+  block_min_max<G>(mn, mx, sc, kmin, kmax);
+  if (kmin == kmax) {
+    // every frontier key is equal: any k entries complete the selection
+    const uint32_t base = sl.n_out;
+    for (uint32_t p = tid; p < k; p += G::kThreads)
+      if (base + p < (uint32_t)K) out_row[base + p] = (int32_t)F.s[p].x;
+    G::sync();
+    if (tid == 0) sl.n_out = base + k;
+    G::sync();
+    return true;
+  }
+  const uint32_t range = kmax - kmin;
+  const int width = 32 - __clz((int)range);  // bits of the range (range >= 1)
+  const int shift = width > 11 ? width - 11 : 0;
+  const int nbins = (int)(((range >> shift) + 1u + 127u) & ~127u);  // <= 2048
+  clear_hist<G>(hist, nbins);
+  G::sync();
+  for (uint32_t p = tid; p < n; p += G::kThreads)
+    smem_add(&hist[(F.s[p].y - kmin) >> shift], 1u);
+  G::sync();
+  find_boundaries<G>(hist, sc, nbins, 1, k, 0u);
+  const int b = sc.res_bin[0];
+  const uint32_t below = sc.res_below[0], cnt = sc.res_cnt[0];
+  const uint32_t kk = k - below;  // keys still wanted from bucket b (1 <= kk <= cnt)
+  const bool whole = b >= 0 && kk == cnt;
+  if (b < 0 || (!whole && cnt > pcap)) {
+    rebuild_h0<G>(F, n, hist);
+    return false;
+  }
+  if (tid == 0) sc.bcast = 0;
+  G::sync();
+  uint32_t* ckey = scratch;
+  int32_t* cidx = reinterpret_cast<int32_t*>(scratch + pcap);
+  for (uint32_t p0 = 0; p0 < nr; p0 += G::kThreads) {
+    const uint32_t p = p0 + tid;
+    const bool in = p < n;
+    uint2 e = make_uint2(0u, 0xFFFFFFFFu);
+    if (in) e = F.s[p];
+    const uint32_t bin = (e.y - kmin) >> shift;
+    const bool com = in && (bin < (uint32_t)b || (whole && bin == (uint32_t)b));
+    commit_warp(&sl.n_out, out_row, K, com, (int32_t)e.x, lt);
+    if (!whole) {
+      const bool col = in && bin == (uint32_t)b;
+      const uint32_t bal = __ballot_sync(kFull, col);
+      if (bal != 0u) {
+        uint32_t base = 0u;
+        if ((tid & 31) == 0) base = (uint32_t)atomicAdd(&sc.bcast, __popc(bal));
+        base = __shfl_sync(kFull, base, 0);
+        if (col) {
+          const uint32_t slot = base + (uint32_t)__popc(bal & lt);
+          ckey[slot] = e.y;
+          cidx[slot] = (int32_t)e.x;
+        }
+      }
+    }
+  }
+  G::sync();
+  if (whole) return true;
+  if (cnt <= 32u) {
+    // One warp ranks the bucket: a key's rank counts the smaller keys and
+    // the equal keys in lower lanes, so exactly kk lanes take.
+    if (tid < 32) {
+      const bool valid = (uint32_t)tid < cnt;
+      const uint32_t x = valid ? ckey[tid] : 0xFFFFFFFFu;
+      const int32_t xi = valid ? cidx[tid] : -1;
+      uint32_t rank = 0u;
+      for (int j = 0; j < 32; ++j) {
+        const uint32_t y = __shfl_sync(kFull, x, j);
+        if ((uint32_t)j < cnt && (y < x || (y == x && j < tid))) ++rank;
+      }
+      commit_warp(&sl.n_out, out_row, K, valid && rank < kk, xi, lt);
+    }
+    G::sync();
+    return true;
+  }
+  uint32_t below1;
+  bool bad = false;
+  const uint32_t vstar = small_select<G>(ckey, cnt, 0xFFFFFFFFu, kk, hist, sc, below1, bad);
+  if (bad) {  // inconsistent counts: cannot happen; finish_row flags it
+    G::sync();
+    return true;
+  }
+  const uint32_t ties = kk - below1;
+  if (tid == 0) sl.n_keep = 0u;
+  G::sync();
+  const uint32_t cr = (cnt + 31u) & ~31u;
+  for (uint32_t p0 = 0; p0 < cr; p0 += G::kThreads) {
+    const uint32_t p = p0 + tid;
+    const bool in = p < cnt;
+    const uint32_t d = in ? ckey[p] : 0xFFFFFFFFu;
+    const bool com = in && d < vstar;
+    const bool tie = in && d == vstar;
+    const uint32_t tb = __ballot_sync(kFull, tie);
+    bool take = false;
+    if (tb) {
+      uint32_t base = 0u;
+      if ((tid & 31) == 0) base = atomicAdd(&sl.n_keep, (uint32_t)__popc(tb));
+      base = __shfl_sync(kFull, base, 0);
+      take = tie && base + (uint32_t)__popc(tb & lt) < ties;
+    }
+    commit_warp(&sl.n_out, out_row, K, com || take, in ? cidx[p] : -1, lt);
+  }
+  G::sync();
+  return true;
+}
+
+// Phase 3 of a row: the range-relative form above when the frontier is in
+// shared memory and its boundary bucket fits `scratch` (scap words), the
+// fixed 11+11+10 digits of eqs. 22-25 otherwise.
+template <class G>
+__device__ void refine(const Frontier& F, uint32_t n, uint32_t k, uint32_t* hist,
+                       GroupScratch& sc, Slot& sl, int32_t* out_row, int K, uint32_t* scratch,
+                       uint32_t scap) {
+  if (n <= F.cap && refine_fast<G>(F, n, k, hist, sc, sl, out_row, K, scratch, scap / 2u))
+    return;
+  refine_digits<G>(F, n, k, hist, sc, sl, out_row, K, scratch, scap);
 }
 
 // ----------------------------------------------------------------------------
@@ -1594,24 +1753,41 @@ struct ViewDma {
 // row whose capacity N is not a multiple of s) are loaded directly, as are all
 // of them once a copy has timed out.  Entered with a cleared histogram; leaves
 // it dirty.
+// View entries of row r (length L, phase a) that the TMA boxes cover, and the
+// number of boxes.
+__device__ __forceinline__ int view_boxes(const Params& p, int L, int a, int& covered) {
+  const int nv = view_size(L, a, p.s);
+  const int box = p.view_box;
+  covered = min(min(nv, p.N / p.s), (int)kViewBoxes * box);
+  return (covered + box - 1) / box;
+}
+
+// Issues the view boxes of row r (one thread); false when nothing was issued.
+__device__ __forceinline__ bool view_tma_issue(const Params& p, int r, int L, int a,
+                                               const ViewDma& vd) {
+  int covered;
+  const int nq = view_boxes(p, L, a, covered);
+  if ((*vd.phase & 2u) != 0u || nq <= 0) return false;
+  // earlier generic reads of the buffer are ordered before the copies
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  mbar_expect_tx(vd.bar, (uint32_t)nq * (uint32_t)p.view_box * 16u);
+  for (int q = 0; q < nq; ++q)
+    tma_load_3d(smem_addr(vd.buf) + (uint32_t)q * 4096u, &p.view_map, a & ~3, q * p.view_box, r,
+                vd.bar);
+  return true;
+}
+
 template <class G>
 __device__ void sample_view_tma(const Params& p, int r, const float* row, int L, int a,
                                 uint32_t* hist, GroupScratch& sc, Slot& sl, const ViewDma& vd) {
   const int nv = view_size(L, a, p.s);
   const int tid = G::rank();
   const int box = p.view_box;
-  const int lines = p.N / p.s;
-  const int covered = min(min(nv, lines), (int)kViewBoxes * box);
-  const int nq = (covered + box - 1) / box;
+  int covered;
+  (void)view_boxes(p, L, a, covered);
   if (tid == 0) {
     int ok = 0;
-    if ((*vd.phase & 2u) == 0u && nq > 0) {
-      // earlier generic reads of the buffer are ordered before the copies
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_expect_tx(vd.bar, (uint32_t)nq * (uint32_t)box * 16u);
-      for (int q = 0; q < nq; ++q)
-        tma_load_3d(smem_addr(vd.buf) + (uint32_t)q * 4096u, &p.view_map, a & ~3, q * box, r,
-                    vd.bar);
+    if (view_tma_issue(p, r, L, a, vd)) {
       const uint32_t ph = *vd.phase & 1u;
       if (mbar_wait_parity_bounded(vd.bar, ph)) {
         *vd.phase = ph ^ 1u;
