@@ -32,10 +32,12 @@ constexpr int kPersistentThreads = ETK_PERSISTENT_THREADS;
 constexpr int kKvSplitThreads = 512;
 constexpr int kRowLocalThreads = 1024;
 constexpr int kClusterThreads = 512;
-// Scores of one row segment resident in a cluster CTA's shared memory, and
-// the largest cluster (the portable limit).
+// Cluster split: scores of a row segment held in a CTA's shared memory, the
+// longest segment of one CTA (the rest read from global memory), and the
+// largest cluster (16: above the portable limit of 8, allowed per kernel).
 constexpr int kClusterStage = 16384;
-constexpr int kClusterMaxSplits = 8;
+constexpr int kClusterSegment = 2 * kClusterStage;
+constexpr int kClusterMaxSplits = 16;
 constexpr int kPersistentCap = ETK_PERSISTENT_CAP;
 constexpr int kKvSplitCap = 4096;
 constexpr int kRowLocalCap = 8192;

@@ -163,7 +163,13 @@ int exact_topk_make_plan(int64_t num_rows, int64_t max_kv_len, int64_t row_pitch
   //   unless the KV-split would give each row a single segment: the
   //   persistent kernel then runs the same one-CTA-per-row work faster.
   // - Persistent sampled otherwise.
-  const int64_t cluster_P = ceil_div64(max_kv_len, kClusterStage);
+  // Cluster split: the fewest CTAs that hold the row in shared memory, up to
+  // 16; rows up to 16 * kClusterSegment scores leave the rest of each
+  // segment in global memory.
+  const int64_t cluster_min_P = ceil_div64(max_kv_len, kClusterSegment);
+  const int64_t held_P = ceil_div64(max_kv_len, kClusterStage);
+  const int64_t cluster_P = held_P < kClusterMaxSplits ? held_P : kClusterMaxSplits;
+  const bool cluster_fits = cluster_min_P <= kClusterMaxSplits;
   const int64_t rowlocal_wave =
       (int64_t)info->sm_count * (info->rowlocal_ctas_per_sm > 0 ? info->rowlocal_ctas_per_sm : 1);
   const int64_t kv_target =
@@ -175,7 +181,12 @@ int exact_topk_make_plan(int64_t num_rows, int64_t max_kv_len, int64_t row_pitch
                    ? EXACT_TOPK_FAMILY_PERSISTENT_SAMPLED
                    : EXACT_TOPK_FAMILY_ROW_LOCAL_EXACT;
     else if (num_rows < info->sm_count)
-      family = (cluster_P <= kClusterMaxSplits && info->cluster_ctas_per_sm > 0 &&
+      // The planner takes clusters of up to 8 CTAs (rows up to 131072 scores,
+      // held in shared memory).  Clusters of up to 16, whose segments read
+      // their second half from global memory, run on request: on the few
+      // long rows workload (8 x 524288) they measured 35.4 us against 30.9 us
+      // for the KV-split.
+      family = (cluster_fits && cluster_P <= 8 && info->cluster_ctas_per_sm > 0 &&
                 num_rows * cluster_P <= 2LL * info->sm_count * info->cluster_ctas_per_sm)
                    ? EXACT_TOPK_FAMILY_CLUSTER_SPLIT
                    : (num_rows >= kv_target ? EXACT_TOPK_FAMILY_PERSISTENT_SAMPLED
@@ -248,9 +259,9 @@ int exact_topk_make_plan(int64_t num_rows, int64_t max_kv_len, int64_t row_pitch
     p.splits = (int32_t)P;
     p.workers = (int32_t)(num_rows * P);
   } else if (family == EXACT_TOPK_FAMILY_CLUSTER_SPLIT) {
-    // The fewest CTAs whose shared memory holds the widest row.
     const int64_t P = r.splits ? r.splits : cluster_P;
-    if (P < cluster_P || P > kClusterMaxSplits || num_rows > 65535) return EXACT_TOPK_ERR_BAD_PLAN;
+    if (P < cluster_min_P || P > kClusterMaxSplits || num_rows > 65535)
+      return EXACT_TOPK_ERR_BAD_PLAN;
     p.splits = (int32_t)P;
     p.workers = (int32_t)(num_rows * P);
   } else {
@@ -308,7 +319,7 @@ int check_run(const exact_topk_plan* plan, const float* logits, const int32_t* k
     return EXACT_TOPK_ERR_BAD_PLAN;
   if (plan->family == EXACT_TOPK_FAMILY_CLUSTER_SPLIT &&
       (plan->num_rows > 65535 || plan->splits > kClusterMaxSplits ||
-       (int64_t)plan->splits * kClusterStage < plan->max_kv_len ||
+       (int64_t)plan->splits * kClusterSegment < plan->max_kv_len ||
        (int64_t)plan->workers != plan->num_rows * plan->splits))
     return EXACT_TOPK_ERR_BAD_PLAN;
   const int expect_cap = plan->family == EXACT_TOPK_FAMILY_PERSISTENT_SAMPLED

@@ -239,6 +239,15 @@ __device__ __forceinline__ void ld_stream8(const float* p, uint32_t* x) {
       : "l"(p));
 }
 
+// 128-bit read-once load of 4 score bit patterns (16-byte aligned address).
+__device__ __forceinline__ uint4 ldg_v4(const float* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
+}
+
 __device__ __forceinline__ uint32_t ld_stream1(const float* p) {
   uint32_t v;
   asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
@@ -941,20 +950,28 @@ __device__ __forceinline__ void hist_add_same(uint32_t* hist, uint32_t bin, bool
 // range [min, max] (so that clustered values still spread over the bins).
 // Returns the value and, in `below`, how many considered values are smaller;
 // `bad` when no value is considered or the counts are inconsistent.
+// With `range_lo` <= every considered value (and vhi >= every one), the
+// range [range_lo, vhi] is taken as given instead of measured by a pass.
 template <class G>
 __device__ uint32_t small_select(const uint32_t* v, uint32_t n, uint32_t vhi, uint32_t t,
-                                 uint32_t* hist, GroupScratch& sc, uint32_t& below, bool& bad) {
+                                 uint32_t* hist, GroupScratch& sc, uint32_t& below, bool& bad,
+                                 bool have_range = false, uint32_t range_lo = 0u) {
   const int tid = G::rank();
-  uint32_t mn = 0xFFFFFFFFu, mx = 0u;
-  for (uint32_t i = tid; i < n; i += G::kThreads) {
-    const uint32_t x = v[i];
-    if (x <= vhi) {
-      mn = min(mn, x);
-      mx = max(mx, x);
-    }
-  }
   uint32_t kmin, kmax;
-  block_min_max<G>(mn, mx, sc, kmin, kmax);
+  if (have_range) {
+    kmin = range_lo;
+    kmax = vhi;
+  } else {
+    uint32_t mn = 0xFFFFFFFFu, mx = 0u;
+    for (uint32_t i = tid; i < n; i += G::kThreads) {
+      const uint32_t x = v[i];
+      if (x <= vhi) {
+        mn = min(mn, x);
+        mx = max(mx, x);
+      }
+    }
+    block_min_max<G>(mn, mx, sc, kmin, kmax);
+  }
   below = 0u;
   bad = kmin > kmax;
   if (bad) return 0u;
@@ -2324,7 +2341,8 @@ struct ClusterState {
   uint32_t n_out;      // leader: output slots handed out
   uint32_t n_keep;     // leader: tie slots handed out
   int32_t timed_out;   // the segment copy did not complete in time
-  int32_t pad_[5];
+  uint32_t kmin;       // smallest admitted key (d <= T1) in this segment
+  int32_t pad_[4];
   uint32_t wcnt[16];   // admitted keys (d <= T1) found by each warp
   uint32_t pad2_[16];
 };
@@ -2402,6 +2420,9 @@ __device__ __forceinline__ uint32_t atom_add_peer(uint32_t a, uint32_t v) {
   asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(a), "r"(v) : "memory");
   return old;
 }
+__device__ __forceinline__ void red_add_peer(uint32_t a, uint32_t v) {
+  asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
 // Sums histogram `local` (nbins, a multiple of 4, at most 4 per thread) over
 // the P CTAs of the cluster into `sum`.  Group barrier before return.
 template <class G>
@@ -2463,64 +2484,80 @@ struct Cut {
 };
 
 // Phase 3 over the cluster for rows whose frontier does not fit a merged
-// list (tie-heavy rows, exact coarse recovery): 11+11+10 digits of the key,
-// each round's histogram summed over the cluster through DSMEM.  `xa` and
-// `xc` alternate as the published buffer; `sum` is private.
-template <class G>
-__device__ Cut cluster_select(const uint4* st4, int n, const KeyBand& F, uint32_t k, uint32_t* xa,
-                              uint32_t* xc, uint32_t* sum, GroupScratch& sc, int P) {
+// list (tie-heavy rows, exact coarse recovery).  Each round histograms an
+// 11-bit digit taken over the candidate key interval [qlo, qhi) (initially
+// the frontier's interval: (F.lo, F.hi], or [lo_hint, F.hi] without a lower
+// bound), sums it over the cluster through DSMEM and narrows the interval to
+// the boundary bucket; the threshold is the one eqs. 22-25 reach with fixed
+// 11+11+10 digits.  A frontier inside one coarse bin (exact recovery) spans
+// about 2^18 keys and resolves in two rounds.  `xa` and `xc` alternate as the
+// published buffer; `sum` is private.
+template <class G, class Vec>
+__device__ Cut cluster_select(const Vec& seg_vec, int n, const KeyBand& F, uint32_t k,
+                              uint32_t* xa, uint32_t* xc, uint32_t* sum, GroupScratch& sc, int P,
+                              uint32_t lo_hint) {
   const int tid = G::rank();
   const int nv4 = (n + 3) >> 2;
   Cut cut{0, 0u, 0u, false};
-  uint32_t prefix = 0u;
+  uint64_t qlo = F.has_lo ? (uint64_t)F.lo + 1u : (uint64_t)lo_hint;  // inclusive
+  uint64_t qhi = (uint64_t)F.hi + 1u;                                  // exclusive
   uint32_t* nxt = xa;
-  for (int j = 0; j < 3; ++j) {
-    const int width = j == 2 ? 10 : 11;
-    const int shift = j == 0 ? 21 : (j == 1 ? 10 : 0);
-    const int pshift = shift + width;  // digits above j
-    clear_hist<G>(nxt, kCoarseBins);
+  for (int round = 0; round < 4; ++round) {  // 32 bits in 11-bit digits: 3 rounds suffice
+    if (qhi <= qlo) {
+      cut.bad = true;
+      return cut;
+    }
+    if (qhi - qlo == 1u) {
+      // one key value left: the k remaining entries are ties (eq. 25)
+      cut.commit_below = qlo;
+      cut.tie_key = (uint32_t)qlo;
+      cut.ties = k;
+      return cut;
+    }
+    const int bits = 64 - __clzll((long long)(qhi - qlo - 1u));
+    const int width = bits < 11 ? bits : 11;
+    const int shift = bits - width;
+    const int nbins = (1 << width) < 128 ? 128 : (1 << width);
+    clear_hist<G>(nxt, nbins);
     G::sync();
     {
-      const uint32_t top = j == 0 ? 0xFFFFFFFFu
-                                  : (uint32_t)((((uint64_t)prefix + 1u) << pshift) - 1u);
-      const Screen scr(top < F.hi ? top : F.hi);
+      const Screen scr((uint32_t)(qhi - 1u));
       RunHist rh;
       for (int t = tid; t < nv4; t += G::kThreads) {
-        const uint4 v = st4[t];
+        const uint4 v = seg_vec(t);
         if (!scr.any(v)) continue;
         const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const uint32_t d = desc_key(u[e]);
-          if (4 * t + e < n && F.in(d) && (j == 0 || (d >> pshift) == prefix))
-            rh.add(nxt, digit(d, j));
+          if (4 * t + e < n && (uint64_t)d >= qlo && (uint64_t)d < qhi)
+            rh.add(nxt, (uint32_t)(((uint64_t)d - qlo) >> shift));
         }
       }
       rh.flush(nxt);
     }
     G::sync();
     cluster_sync_all();
-    cluster_hist_sum<G>(nxt, sum, 1 << width, P);
+    cluster_hist_sum<G>(nxt, sum, nbins, P);
     nxt = nxt == xa ? xc : xa;
-    find_boundaries<G>(sum, sc, 1 << width, 1, k, 0u);
+    find_boundaries<G>(sum, sc, nbins, 1, k, 0u);
     const int b = sc.res_bin[0];
     const uint32_t below = sc.res_below[0], cnt = sc.res_cnt[0];
     if (b < 0) {
       cut.bad = true;
       return cut;
     }
-    prefix = (prefix << width) | (uint32_t)b;
+    qlo += (uint64_t)b << shift;
+    const uint64_t top = qlo + ((uint64_t)1 << shift);
+    qhi = top < qhi ? top : qhi;
     if (below + cnt == k) {
-      cut.commit_below = (uint64_t)(prefix + 1u) << shift;
+      // the boundary bucket closes the quota: every key below its end
+      cut.commit_below = qhi;
       return cut;
     }
     k -= below;
-    if (j == 2) {
-      cut.commit_below = prefix;
-      cut.tie_key = prefix;
-      cut.ties = k;
-    }
   }
+  cut.bad = true;
   return cut;
 }
 
@@ -2575,6 +2612,8 @@ __device__ void cluster_commit(const Visit& visit, uint64_t commit_below, uint32
 __global__ void __launch_bounds__(kClusterThreads, 2) cluster_split_kernel(Params p) {
   using G = CtaGroup<kClusterThreads>;
   static_assert(kClusterThreads / 32 == 16, "the merged-list table assumes 16 warps per CTA");
+  static_assert(16 * kClusterMaxSplits <= 256 && (16 * kClusterMaxSplits) % 32 == 0,
+                "sub-list table of 256 entries");
   unsigned char* sm = smem_base();
   constexpr ClusterLayout lay = cluster_layout();
   ClusterState& cs = *reinterpret_cast<ClusterState*>(sm + lay.state);
@@ -2609,14 +2648,18 @@ __global__ void __launch_bounds__(kClusterThreads, 2) cluster_split_kernel(Param
   }
   int lo, hi;
   segment_bounds(L, P, (int)q, lo, hi);
-  int n = hi - lo;  // <= kClusterStage by the plan (checked on the host)
-  if (n > kClusterStage) {
-    n = kClusterStage;  // never taken for a valid plan; the row's result is flagged
+  int n = hi - lo;  // <= kClusterSegment by the plan (checked on the host)
+  if (n > kClusterSegment) {
+    n = kClusterSegment;  // never taken for a valid plan; the row's result is flagged
     if (threadIdx.x == 0) flag_status(p.counters, 1);
   }
   const float* src = row + lo;
   const bool bulk = (reinterpret_cast<uintptr_t>(src) & 15u) == 0u;
-  const int nb = bulk ? (n & ~3) : 0;  // scores moved by the bulk copy
+  // The first `held` scores of the segment are held in shared memory; the
+  // rest (segments longer than kClusterStage) are read from global memory,
+  // prefetched into L2 while Phase 1 runs.
+  const int held = n < kClusterStage ? n : kClusterStage;
+  const int nb = bulk ? (held & ~3) : 0;  // scores moved by the bulk copy
   const uint32_t bar = smem_addr(&cs.bar);
 
   // Phase-1 view (eq. 13), replicated in every CTA of the cluster as in the
@@ -2625,12 +2668,22 @@ __global__ void __launch_bounds__(kClusterThreads, 2) cluster_split_kernel(Param
   const int a = view_phase(r, p.s, p.s_bits);
   const int vsize = view_size(L, a, p.s);
   const bool sampled = p.prev == nullptr && vsize >= (p.dual ? p.q1 : p.q0);
-  constexpr int kViewAhead = 4;  // view loads per thread issued before the copy
+  // Small clusters replicate the view in every CTA; clusters of more than
+  // four CTAs split it: each CTA loads the view entries inside its own
+  // segment and adds them into the leader's histogram (the union over the
+  // segments is the row's view, eq. 13).
+  const bool split_view = sampled && P > 4;
+  int vt0 = 0, vt1 = vsize;  // view entries t in [vt0, vt1) handled here
+  if (split_view) {
+    vt0 = lo <= a ? 0 : (lo - a + p.s - 1) / p.s;
+    vt1 = hi <= a ? 0 : min(vsize, (hi - a + p.s - 1) / p.s);
+  }
+  constexpr int kViewAhead = 8;  // view loads per thread issued before the copy
   uint32_t vu[kViewAhead];
 #pragma unroll
   for (int k = 0; k < kViewAhead; ++k) {
-    const int t = k * G::kThreads + tid;
-    vu[k] = (sampled && t < vsize)
+    const int t = vt0 + k * G::kThreads + tid;
+    vu[k] = (sampled && t < vt1)
                 ? __ldg(reinterpret_cast<const unsigned int*>(row) + a + (int64_t)t * p.s)
                 : 0u;
   }
@@ -2646,15 +2699,18 @@ __global__ void __launch_bounds__(kClusterThreads, 2) cluster_split_kernel(Param
   if (tid == 0) {
     mbar_init(bar, 1u);
     if (nb > 0 && !copy_late) bulk_copy_g2s(smem_addr(stage), src, (uint32_t)nb * 4u, bar);
+    const uint32_t tail_bytes = (uint32_t)(n - held) * 4u & ~15u;
+    if (bulk && tail_bytes > 0u) prefetch_l2(src + held, tail_bytes);
     cs.cnt_a = 0u;
     cs.cnt_b = 0u;
     cs.n_out = 0u;
     cs.n_keep = 0u;
     cs.timed_out = 0;
+    cs.kmin = 0xFFFFFFFFu;
     sl.tau0 = -1;
     sl.tau1 = -1;
   }
-  for (int t = nb + tid; t < n; t += G::kThreads) stage[t] = ld_stream1(src + t);
+  for (int t = nb + tid; t < held; t += G::kThreads) stage[t] = ld_stream1(src + t);
 
   // ---- Phase 1 ----
   // Every CTA histograms the whole row's view (replicated, as the KV-split of
@@ -2666,7 +2722,32 @@ __global__ void __launch_bounds__(kClusterThreads, 2) cluster_split_kernel(Param
   } else {
     direct = vsize < (p.dual ? p.q1 : p.q0);
   }
-  if (!guess && !direct) {
+  if (!guess && !direct && split_view) {
+    // Every CTA clears its exchange histogram before any CTA adds into the
+    // leader's (first cluster barrier); the second orders the adds before
+    // the reads.
+    clear_hist<G>(xC, kCoarseBins);
+    G::sync();
+    cluster_sync_all();
+    const uint32_t lead = peer_addr(smem_addr(xC), 0u);
+#pragma unroll
+    for (int k = 0; k < kViewAhead; ++k) {
+      const int t = vt0 + k * G::kThreads + tid;
+      if (t < vt1) red_add_peer(lead + 4u * (uint32_t)coarse_bin(vu[k]), 1u);
+    }
+    for (int t = vt0 + kViewAhead * G::kThreads + tid; t < vt1; t += G::kThreads)
+      red_add_peer(lead + 4u * (uint32_t)coarse_bin(__ldg(reinterpret_cast<const unsigned int*>(row) +
+                                                          a + (int64_t)t * p.s)),
+                   1u);
+    G::sync();
+    cluster_sync_all();
+    reinterpret_cast<uint4*>(sum)[tid] = ld_peer4(lead + 16u * (uint32_t)tid);
+    static_assert(kCoarseBins == 4 * kClusterThreads, "one 4-bin vector per thread");
+    G::sync();
+    if (copy_late && tid == 0 && nb > 0)
+      bulk_copy_g2s(smem_addr(stage), src, (uint32_t)nb * 4u, bar);
+    view_cutoffs<G>(p, sum, sc, sl);
+  } else if (!guess && !direct) {
     clear_hist<G>(sum, kCoarseBins);
     G::sync();
 #pragma unroll
@@ -2695,6 +2776,19 @@ __global__ void __launch_bounds__(kClusterThreads, 2) cluster_split_kernel(Param
   G::sync();
   const uint4* st4 = reinterpret_cast<const uint4*>(stage);
   const int nv4 = (n + 3) >> 2;
+  const int nh4 = (held + 3) >> 2;  // vectors held in shared memory
+  // Scores 4t .. 4t+3 of the segment (positions >= n are junk for the caller
+  // to mask): from shared memory below `held`, else from global memory.
+  auto seg_vec = [&](int t) -> uint4 {
+    if (t < nh4) return st4[t];
+    if (bulk) return ldg_v4(src + 4 * t);
+    uint4 v;
+    v.x = 4 * t < n ? ld_stream1(src + 4 * t) : 0u;
+    v.y = 4 * t + 1 < n ? ld_stream1(src + 4 * t + 1) : 0u;
+    v.z = 4 * t + 2 < n ? ld_stream1(src + 4 * t + 2) : 0u;
+    v.w = 4 * t + 3 < n ? ld_stream1(src + 4 * t + 3) : 0u;
+    return v;
+  };
 
   // ---- Phase 2 over the resident segment (one pass) ----
   // Both classes are counted per thread; every admitted key (d <= T1) and its
@@ -2707,16 +2801,20 @@ __global__ void __launch_bounds__(kClusterThreads, 2) cluster_split_kernel(Param
     uint32_t ca = 0u;   // this lane's class-A keys
     uint32_t* wk = keys + warp * kRegionCap;
     uint16_t* wp = pos + warp * kRegionCap;
-    const int nv4r = (nv4 + 31) & ~31;
-    for (int t = tid; t < nv4r; t += G::kThreads) {
-      uint4 v = make_uint4(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu);
-      if (t < nv4) v = st4[t];
+    // Called by whole warps; `ok` false for vectors past the segment.  A
+    // warp whose 32 vectors hold no admissible score skips the per-score
+    // ballots.
+    const Screen scr1(T1);
+    uint32_t kmn = 0xFFFFFFFFu;  // this lane's smallest admitted key
+    auto classify = [&](const uint4& v, int t, bool ok) {
+      if (__ballot_sync(kFull, ok && scr1.any(v)) == 0u) return;
       const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const uint32_t d = desc_key(u[e]);
-        const bool adm = t < nv4 && 4 * t + e < n && d <= T1;
+        const bool adm = ok && 4 * t + e < n && d <= T1;
         ca += (adm && d <= T0) ? 1u : 0u;
+        if (adm) kmn = min(kmn, d);
         const uint32_t bal = __ballot_sync(kFull, adm);
         if (bal != 0u) {
           const uint32_t rk = wc + (uint32_t)__popc(bal & lt);
@@ -2727,12 +2825,33 @@ __global__ void __launch_bounds__(kClusterThreads, 2) cluster_split_kernel(Param
           wc += (uint32_t)__popc(bal);
         }
       }
+    };
+    const uint4 none = make_uint4(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu);
+    const int nh4r = (nh4 + 31) & ~31;
+    for (int t = tid; t < nh4r; t += G::kThreads) classify(t < nh4 ? st4[t] : none, t, t < nh4);
+    // the part read from global memory: four vectors per thread in flight
+    const int ntail = nv4 - nh4;
+    const int ntr = (ntail + 31) & ~31;
+    for (int b0 = 0; b0 < ntr; b0 += 4 * G::kThreads) {
+      uint4 v[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int j = b0 + k * G::kThreads + tid;
+        v[k] = j < ntail ? seg_vec(nh4 + j) : none;
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int j = b0 + k * G::kThreads + tid;
+        if (b0 + k * G::kThreads + 32 * warp < ntr) classify(v[k], nh4 + j, j < ntail);
+      }
     }
     ca = __reduce_add_sync(kFull, ca);
+    kmn = __reduce_min_sync(kFull, kmn);
     if (lane == 0) {
       cs.wcnt[warp] = wc;
       atomicAdd(&cs.cnt_a, ca);
       atomicAdd(&cs.cnt_b, wc - ca);
+      if (kmn != 0xFFFFFFFFu) atomicMin(&cs.kmin, kmn);
     }
   } else if (lane == 0) {
     cs.wcnt[warp] = 0u;
@@ -2744,15 +2863,19 @@ __global__ void __launch_bounds__(kClusterThreads, 2) cluster_split_kernel(Param
   // list: sub-list 16 j + w is warp w's region in CTA j, and h256[16 j + w]
   // its offset.  One warp issues every peer load at once.
   if (warp == 0) {
-    uint32_t ca = 0u, cb = 0u;
+    uint32_t ca = 0u, cb = 0u, km = 0xFFFFFFFFu;
     if (lane < P) {
       ca = ld_peer(peer_addr(smem_addr(&cs.cnt_a), (uint32_t)lane));
       cb = ld_peer(peer_addr(smem_addr(&cs.cnt_b), (uint32_t)lane));
+      km = ld_peer(peer_addr(smem_addr(&cs.kmin), (uint32_t)lane));
     }
-    uint32_t c[4];
+    km = __reduce_min_sync(kFull, km);
+    // 16 sub-lists per CTA, kSub per lane: 16 * kClusterMaxSplits in all
+    constexpr int kSub = 16 * kClusterMaxSplits / 32;
+    uint32_t c[kSub];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int rr = 4 * lane + i, j = rr >> 4, w = rr & 15;
+    for (int i = 0; i < kSub; ++i) {
+      const int rr = kSub * lane + i, j = rr >> 4, w = rr & 15;
       c[i] = j < P ? ld_peer(peer_addr(smem_addr(&cs.wcnt[w]), (uint32_t)j)) : 0u;
     }
     ca = __reduce_add_sync(kFull, ca);
@@ -2760,7 +2883,7 @@ __global__ void __launch_bounds__(kClusterThreads, 2) cluster_split_kernel(Param
     bool over = false;
     uint32_t s4 = 0u;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < kSub; ++i) {
       over = over || c[i] > (uint32_t)kRegionCap;
       s4 += c[i];
     }
@@ -2772,8 +2895,8 @@ __global__ void __launch_bounds__(kClusterThreads, 2) cluster_split_kernel(Param
     }
     uint32_t run = incl - s4;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      h256[4 * lane + i] = run;
+    for (int i = 0; i < kSub; ++i) {
+      h256[kSub * lane + i] = run;
       run += c[i];
     }
     over = __any_sync(kFull, over);
@@ -2781,6 +2904,7 @@ __global__ void __launch_bounds__(kClusterThreads, 2) cluster_split_kernel(Param
       sl.c0 = (int)ca;
       sl.c1 = (int)cb;
       sc.bcast = over ? 1 : 0;
+      sc.bcast2 = (int32_t)km;  // smallest admitted key of the row
     }
   }
   G::sync();
@@ -2829,44 +2953,54 @@ __global__ void __launch_bounds__(kClusterThreads, 2) cluster_split_kernel(Param
     // Warp w copies the regions of warp w in every CTA: consecutive keys of
     // one peer region per request, all of a warp's requests in flight together.
     const uint32_t kb = smem_addr(keys);
-    uint32_t vv[kClusterMaxSplits][4];
+    constexpr int kGroup = 4;  // CTAs whose regions are in flight together
+    for (int j0 = 0; j0 < P; j0 += kGroup) {
+      uint32_t vv[kGroup][4];
 #pragma unroll
-    for (int j = 0; j < kClusterMaxSplits; ++j) {
+      for (int g = 0; g < kGroup; ++g) {
+        const int j = j0 + g;
 #pragma unroll
-      for (int x = 0; x < 4; ++x) vv[j][x] = 0u;
-      if (j < P) {
-        const int rr = 16 * j + warp;
-        const uint32_t beg = h256[rr], end = rr + 1 < 16 * P ? h256[rr + 1] : total;
+        for (int x = 0; x < 4; ++x) vv[g][x] = 0u;
+        if (j < P) {
+          const int rr = 16 * j + warp;
+          const uint32_t beg = h256[rr], end = rr + 1 < 16 * P ? h256[rr + 1] : total;
 #pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          const uint32_t e = (uint32_t)lane + 32u * x;
-          if (beg + e < end)
-            vv[j][x] = ld_peer(peer_addr(kb + 4u * ((uint32_t)warp * kRegionCap + e), (uint32_t)j));
+          for (int x = 0; x < 4; ++x) {
+            const uint32_t e = (uint32_t)lane + 32u * x;
+            if (beg + e < end)
+              vv[g][x] =
+                  ld_peer(peer_addr(kb + 4u * ((uint32_t)warp * kRegionCap + e), (uint32_t)j));
+          }
         }
       }
-    }
 #pragma unroll
-    for (int j = 0; j < kClusterMaxSplits; ++j) {
-      if (j < P) {
-        const int rr = 16 * j + warp;
-        const uint32_t beg = h256[rr], end = rr + 1 < 16 * P ? h256[rr + 1] : total;
+      for (int g = 0; g < kGroup; ++g) {
+        const int j = j0 + g;
+        if (j < P) {
+          const int rr = 16 * j + warp;
+          const uint32_t beg = h256[rr], end = rr + 1 < 16 * P ? h256[rr + 1] : total;
 #pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          const uint32_t e = (uint32_t)lane + 32u * x;
-          if (beg + e < end) sumx[beg + e] = vv[j][x];
+          for (int x = 0; x < 4; ++x) {
+            const uint32_t e = (uint32_t)lane + 32u * x;
+            if (beg + e < end) sumx[beg + e] = vv[g][x];
+          }
         }
       }
     }
     G::sync();
     uint32_t below;
     bool bad = false;
-    const uint32_t vstar = small_select<G>(sumx, total, F.hi, k, hist, sc, below, bad);
+    // every gathered key lies in [smallest admitted key, F.hi] or above F.hi
+    const uint32_t kmin_row = (uint32_t)sc.bcast2;
+    const uint32_t vstar = small_select<G>(sumx, total, F.hi, k, hist, sc, below, bad,
+                                           kmin_row <= F.hi, kmin_row);
     cut.bad = bad;
     cut.commit_below = vstar;
     cut.tie_key = vstar;
     cut.ties = k - below;
   } else if (!recover) {
-    cut = cluster_select<G>(st4, n, F, k, xA, xC, sum, sc, P);
+    const uint32_t kmin_row = (uint32_t)sc.bcast2;  // smallest admitted key of the row
+    cut = cluster_select<G>(seg_vec, n, F, k, xA, xC, sum, sc, P, kmin_row <= F.hi ? kmin_row : 0u);
   } else {
     // Exact coarse recovery (eq. 20) over the resident row: coarse histogram,
     // tau* = min{b : C(b) >= K}, E0 = {c < tau*}, Q0 = {c == tau*}.
@@ -2875,7 +3009,7 @@ __global__ void __launch_bounds__(kClusterThreads, 2) cluster_split_kernel(Param
     {
       RunHist rh;
       for (int t = tid; t < nv4; t += G::kThreads) {
-        const uint4 v = st4[t];
+        const uint4 v = seg_vec(t);
         const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e)
@@ -2898,7 +3032,7 @@ __global__ void __launch_bounds__(kClusterThreads, 2) cluster_split_kernel(Param
     if (tstar < 0)
       cut.bad = true;
     else
-      cut = cluster_select<G>(st4, n, F, k, xC, xA, sum, sc, P);
+      cut = cluster_select<G>(seg_vec, n, F, k, xC, xA, sum, sc, P, 0u);
   }
   G::sync();  // every thread holds the cut before the commit reuses the scratch
 
@@ -2925,7 +3059,7 @@ __global__ void __launch_bounds__(kClusterThreads, 2) cluster_split_kernel(Param
     const KeyBand FF = F;
     auto visit = [&](auto&& fn) {
       for (int t = tid; t < nv4; t += G::kThreads) {
-        const uint4 v = st4[t];
+        const uint4 v = seg_vec(t);
         const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -2969,6 +3103,11 @@ int set_attrs(KernelT kernel, int family, size_t smem) {
     return EXACT_TOPK_ERR_CUDA;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+    return EXACT_TOPK_ERR_CUDA;
+  // clusters of up to 16 CTAs (the portable limit is 8)
+  if (family == EXACT_TOPK_FAMILY_CLUSTER_SPLIT &&
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+          cudaSuccess)
     return EXACT_TOPK_ERR_CUDA;
   if (cached) g_attr_smem[dev][family] = (int)smem;
   return EXACT_TOPK_OK;
@@ -3118,7 +3257,7 @@ int launch(const exact_topk_plan& plan, const LaunchArgs& a, cudaStream_t stream
       break;
     case EXACT_TOPK_FAMILY_CLUSTER_SPLIT: {
       if (plan.splits < 1 || plan.splits > kClusterMaxSplits ||
-          (int64_t)plan.splits * kClusterStage < plan.max_kv_len)
+          (int64_t)plan.splits * kClusterSegment < plan.max_kv_len)
         return EXACT_TOPK_ERR_BAD_PLAN;
       rc = set_attrs(cluster_split_kernel, EXACT_TOPK_FAMILY_CLUSTER_SPLIT, smem);
       if (rc != EXACT_TOPK_OK) return rc;

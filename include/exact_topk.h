@@ -72,9 +72,11 @@ typedef enum exact_topk_family {
   /* The planner's choice, from the row count M, width N and the device:
      - N < 16384: row-local exact when the rows fit one wave of its CTAs or
        N < 1024, persistent sampled otherwise;
-     - M < SM count: cluster split when a row fits one cluster (N <= 8 * 16384)
-       and the clusters fit about two waves; otherwise the KV-split, unless it
-       would give each row a single segment (persistent sampled then);
+     - M < SM count: cluster split when a row fits the shared memory of a
+       cluster of 8 (N <= 8 * 16384) and the clusters fit about two waves
+       (clusters of up to 16 CTAs, N <= 16 * 32768, on request only);
+       otherwise the KV-split, unless it would give each row a single segment
+       (persistent sampled then);
      - otherwise persistent sampled. */
   EXACT_TOPK_FAMILY_AUTO = 0,
   /* One CTA owns a row for all three phases; rows are claimed from a device
@@ -86,9 +88,11 @@ typedef enum exact_topk_family {
   /* One wide CTA per row takes the exact coarse route directly; short rows stay
      in registers (section 5.5, "Row-local exact"). */
   EXACT_TOPK_FAMILY_ROW_LOCAL_EXACT = 3,
-  /* The P CTAs of one thread-block cluster hold one row in shared memory (at
-     most 16384 scores per CTA, P <= 8); the merge of eq. 27 and every later
-     pass run on chip through distributed shared memory (the KV-split
+  /* The P CTAs of one thread-block cluster (P <= 16) split one row into
+     segments of at most 32768 scores; each CTA holds up to 16384 of them in
+     shared memory (a TMA bulk copy) and reads the rest of its segment from
+     global memory after an L2 prefetch.  The merge of eq. 27 and every later
+     step run on chip through distributed shared memory (the KV-split
      decomposition of section 4.5 for rows that fit a cluster). */
   EXACT_TOPK_FAMILY_CLUSTER_SPLIT = 4
 } exact_topk_family;
@@ -127,8 +131,8 @@ typedef struct exact_topk_plan_request {
   int32_t family;        /* exact_topk_family */
   int32_t stride;        /* view stride s: power of two in [2, 4096] */
   int32_t dual;          /* -1 planner, 0 primary-only, 1 primary + secondary boundary */
-  int32_t splits;        /* segment count P: KV-split [1, 128]; cluster split [1, 8]
-                            with P * 16384 >= max_kv_len */
+  int32_t splits;        /* segment count P: KV-split [1, 128]; cluster split [1, 16]
+                            with P * 32768 >= max_kv_len */
   int32_t workers;       /* persistent / row-local grid size */
   int32_t rho0_num, rho0_den; /* primary retention margin rho (K~ = rho K), default 3/2 */
   int32_t rho1_num, rho1_den; /* secondary margin rho1, default 7/4 */

@@ -57,6 +57,7 @@ def test_version_and_error_strings():
     (8, 140000, 2048, etk.FAMILY_KV_SPLIT, 128, 1),
     (4096, 131072, 2048, etk.FAMILY_PERSISTENT_SAMPLED, 128, 1),
     (8, 524288, 2048, etk.FAMILY_KV_SPLIT, 128, 1),
+    (20, 300000, 2048, etk.FAMILY_KV_SPLIT, 128, 1),
     (256, 131072, 2048, etk.FAMILY_PERSISTENT_SAMPLED, 128, 1),
     (1000, 40000, 2048, etk.FAMILY_PERSISTENT_SAMPLED, 64, 0),
 ])
@@ -80,6 +81,23 @@ def test_planner_families(M, N, K, family, stride, dual):
         assert p.workspace_bytes == 0
 
 
+def test_planner_takes_wide_clusters_on_request():
+    # clusters of up to 16 CTAs hold 16384 scores each and read up to as many
+    # again from global memory: rows up to 16 x 32768 scores
+    p = etk.make_plan(8, 524288, 2048, device_info=GB300, family=etk.FAMILY_CLUSTER_SPLIT)
+    assert (p.splits, p.workers, p.workspace_bytes) == (16, 128, 0)
+    p = etk.make_plan(8, 300000, 2048, device_info=GB300, family=etk.FAMILY_CLUSTER_SPLIT,
+                      splits=10)
+    assert p.splits == 10
+    for bad in (dict(splits=9), dict(splits=17)):
+        with pytest.raises(etk.ExactTopKError) as e:
+            etk.make_plan(8, 300000, 2048, device_info=GB300, family=etk.FAMILY_CLUSTER_SPLIT,
+                          **bad)
+        assert e.value.code == -7
+    with pytest.raises(etk.ExactTopKError):
+        etk.make_plan(8, 524289, 2048, device_info=GB300, family=etk.FAMILY_CLUSTER_SPLIT)
+
+
 def test_planner_overrides_and_errors():
     p = etk.make_plan(10, 100000, 100, device_info=GB300, family=etk.FAMILY_KV_SPLIT, splits=7,
                       stride=32, dual=0, rho0=(5, 4))
@@ -97,7 +115,7 @@ def test_planner_overrides_and_errors():
         assert e.value.code == -3
     for kw in (dict(stride=3), dict(stride=8192), dict(family=9), dict(splits=300,
                family=etk.FAMILY_KV_SPLIT), dict(dual=2), dict(family=etk.FAMILY_CLUSTER_SPLIT,
-               splits=6), dict(family=etk.FAMILY_CLUSTER_SPLIT, splits=9)):
+               splits=3), dict(family=etk.FAMILY_CLUSTER_SPLIT, splits=17)):
         with pytest.raises(etk.ExactTopKError) as e:
             etk.make_plan(4, 100000, 16, device_info=GB300, **kw)
         assert e.value.code == -7

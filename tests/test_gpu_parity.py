@@ -307,7 +307,7 @@ def test_trace_sequence_default_planner():
     # tails, K = min(2048, N / 4)) through the default planner: the calls land
     # on all four kernel families and every row matches the oracle.
     calls = workloads.trace_sequence(1 << 22, 2048, 314, device="cpu",
-                                     widths=(512, 16384, 65536, 262144))
+                                     widths=(512, 16384, 65536, 262144, 1048576))
     families = set()
     for X, ke in calls:
         K = min(2048, X.shape[1] // 4)
@@ -363,3 +363,112 @@ def test_host_errors_launch_nothing():
                           stream) == -6
     torch.cuda.synchronize()
     assert (out.cpu().numpy() == CANARY).all()
+
+
+@pytest.mark.parametrize("splits", [10, 13, 16])
+def test_cluster_split_wide_counts(splits):
+    # Clusters above the portable size of 8 CTAs; segments longer than the
+    # 16384 scores a CTA holds read the rest from global memory.
+    M, N, K = 6, 300000, 2048
+    Xt, ket, K = workloads.generate("long_decode", M=M, N=N, K=K)
+    X, ke = Xt.numpy(), ket.numpy()
+    X = np.where(np.isnan(X), np.float32(0.0), X)
+    ke[:4] = [N, 16385, 270001, 2049]
+    out, tr, plan, ctr = run_gpu(X, ke, K, family=etk.FAMILY_CLUSTER_SPLIT, splits=splits)
+    assert plan.splits == splits
+    compare_rows(X, ke, K, out)
+    assert_counters_zero(ctr)
+    _, tr_ref = oracle_trace_for_plan(X, ke, K, plan)
+    compare_trace(tr, tr_ref)
+
+
+def test_cluster_split_rows_of_524288():
+    # The widest rows a cluster takes (16 CTAs x 32768 scores), with ragged
+    # lengths down to one held segment.
+    M, N, K = 6, 524288, 2048
+    Xt, ket, K = workloads.generate("long_decode", M=M, N=N, K=K, seed=77)
+    X, ke = Xt.numpy(), ket.numpy()
+    X = np.where(np.isnan(X), np.float32(0.0), X)
+    ke[:5] = [N, N - 3, 16 * 16384 + 5, 16384, 300017]
+    out, tr, plan, ctr = run_gpu(X, ke, K, family=etk.FAMILY_CLUSTER_SPLIT)
+    assert plan.splits == 16
+    compare_rows(X, ke, K, out)
+    assert_counters_zero(ctr)
+    _, tr_ref = oracle_trace_for_plan(X, ke, K, plan)
+    compare_trace(tr, tr_ref)
+
+
+def test_cluster_split_wide_unaligned_rows():
+    # Row starts that are only 4-byte aligned: no bulk copy, scalar loads for
+    # the held part and for the part read from global memory.
+    M, N, K = 4, 300001, 1024
+    pitch = N + 1
+    rng = np.random.default_rng(99)
+    flat = rng.standard_normal(M * pitch + 1).astype(np.float32)
+    dev = torch.device("cuda")
+    flat_d = torch.as_tensor(flat).to(dev)
+    Xd = flat_d[1:1 + M * pitch].view(M, pitch)[:, :N]
+    X = Xd.cpu().numpy()
+    ke = np.array([N, 200003, 17, 290000], np.int32)
+    out, tr, plan, ctr = run_gpu(Xd, ke, K, row_pitch=pitch, family=etk.FAMILY_CLUSTER_SPLIT)
+    assert plan.splits == 16
+    compare_rows(X, ke, K, out)
+    assert_counters_zero(ctr)
+    _, tr_ref = oracle_trace_for_plan(X, ke, K, plan)
+    compare_trace(tr, tr_ref)
+
+
+def test_cluster_split_wide_tie_and_constant_rows():
+    # Frontiers far beyond the merged list on wide rows: the cluster-summed
+    # digit rounds and the commit read every segment's global part.
+    M, N, K = 6, 400000, 2048
+    X = np.zeros((M, N), np.float32)
+    X[0] = 0.5
+    X[1] = np.where(np.arange(N) % 3 == 0, 2.0, 1.0)
+    X[2] = np.random.default_rng(5).integers(0, 4, N).astype(np.float32)
+    X[3, :] = -np.inf
+    X[4] = np.random.default_rng(6).standard_normal(N).astype(np.float32)
+    X[4, 390000:] = 7.0                       # a tie band of 10000 maxima in the last segment
+    X[5] = np.where(np.arange(N) % 2 == 0, -0.0, 0.0)
+    ke = np.array([N, N, 399999, 333333, N, 250000], np.int32)
+    out, tr, plan, ctr = run_gpu(X, ke, K, family=etk.FAMILY_CLUSTER_SPLIT)
+    assert plan.splits == 16
+    compare_rows(X, ke, K, out)
+    assert_counters_zero(ctr)
+    _, tr_ref = oracle_trace_for_plan(X, ke, K, plan)
+    compare_trace(tr, tr_ref)
+
+
+@pytest.mark.parametrize("dual", [0, 1])
+def test_cluster_split_wide_forced_routes(dual):
+    # Table 2's routes on rows wide enough for 16-CTA clusters, forced by
+    # planting values on or off the sampled residue class.
+    K, s, N = 64, 16, 400000
+    q0 = -(-3 * K // (2 * s))
+    q1 = -(-7 * K // (4 * s))
+    rng = np.random.default_rng(18)
+    base = rng.standard_normal(N).astype(np.float32)
+
+    def planted(r, off_hi, off_mid):
+        row = base.copy()
+        a = oracle.view_phase(r, s)
+        on = np.arange(a, N, s)
+        off = np.setdiff1d(np.arange(N), on)[::997]  # spread over every segment
+        row[on[:q0]] = 100.0
+        row[on[q0:q1]] = 90.0
+        row[off[:off_hi]] = 100.0
+        row[off[off_hi:off_hi + off_mid]] = 90.0
+        return row
+
+    X = np.stack([base, planted(1, 30, 50), planted(2, 30, 0), base])
+    ke = np.array([N, N, N, 100], np.int32)
+    out, tr, plan, ctr = run_gpu(X, ke, K, family=etk.FAMILY_CLUSTER_SPLIT, stride=s, dual=dual)
+    assert plan.splits == 16
+    compare_rows(X, ke, K, out)
+    assert_counters_zero(ctr)
+    _, tr_ref = oracle_trace_for_plan(X, ke, K, plan)
+    compare_trace(tr, tr_ref)
+    if dual:
+        assert tr[:, 0].tolist() == [1, 2, 3, 5]
+    else:
+        assert tr[:3, 0].tolist() == [1, 4, 4]
