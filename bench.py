@@ -434,7 +434,8 @@ def run_sweep(args):
     with route rates; splits: KV-split segment count P on the few-long-rows
     workload; trace: a serving-style sequence of calls with N growing and
     M = 2^24 / N, each planned by the default planner, timed call by call and
-    as one captured sequence."""
+    as one captured sequence; floor: per workload, a read-only kernel over the
+    valid prefixes beside the selection, in the same replay harness."""
     import math
 
     import torch
@@ -536,6 +537,49 @@ def run_sweep(args):
         emit({"sweep": "trace_sequence", "calls": len(calls), "rows": total_rows,
               "us_per_sequence": sec * 1e6, "rows_per_s": total_rows / sec,
               "gbs": total_alg / sec / 1e9})
+    elif args.sweep == "floor":
+        # The attainable streaming time of each workload: a read-only kernel
+        # over exactly the valid prefixes, in the selection plan's split
+        # count (one segment per row for the single-CTA families), timed
+        # like the selection itself over the same rotated input copies.
+        import workloads as wl
+        peak, _ = hbm_peak()
+        for name in wl.ORDER:
+            c = Case(name, device)
+            sec_sel = median_per_call(c, stream)
+            splits = c.plan.splits if c.plan.family in (2, 4) else 1
+            outs = torch.empty(c.M, splits, dtype=torch.int32, device=device)
+            n = min(1024, max(100, c.copies))
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                etk.stream_floor(c.X[0], c.ke, splits, out=outs, stream=stream)
+                stream.synchronize()
+                with torch.cuda.graph(g, stream=stream):
+                    for k in range(n):
+                        etk.stream_floor(c.X[k % c.copies], c.ke, splits, out=outs, stream=stream)
+            for _ in range(2):
+                g.replay()
+            torch.cuda.synchronize(device)
+            times = []
+            for _ in range(7):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(stream):
+                    e0.record(stream)
+                    g.replay()
+                    e1.record(stream)
+                torch.cuda.synchronize(device)
+                times.append(e0.elapsed_time(e1) / 1e3 / n)
+            sec_floor = sorted(times)[len(times) // 2]
+            score_bytes = c.alg_bytes - c.M * c.K * 4
+            emit({"sweep": "floor", "workload": name, "M": c.M, "N": c.N, "splits": splits,
+                  "family": KERNEL_NAMES[c.plan.family], "floor_us": sec_floor * 1e6,
+                  "floor_frac": score_bytes / sec_floor / 1e9 / peak,
+                  "selection_us": sec_sel * 1e6,
+                  "selection_frac": c.alg_bytes / sec_sel / 1e9 / peak,
+                  "selection_over_floor": sec_sel / sec_floor})
+            del c, outs, g
+            torch.cuda.empty_cache()
     elif args.sweep == "splits":
         X, ke, _ = workloads.generate("long_decode", device=str(device))
         M, N = X.shape
@@ -869,7 +913,8 @@ def parse_args(argv=None):
     ap.add_argument("--stub", action="store_true",
                     help="launcher/aggregation test without a GPU (the line is not a measurement)")
     ap.add_argument("--reference-seconds", type=float, default=60.0)
-    ap.add_argument("--sweep", choices=["crossover", "margins", "splits", "trace"], default=None,
+    ap.add_argument("--sweep", choices=["crossover", "margins", "splits", "trace", "floor"],
+                    default=None,
                     help="planner study instead of the bench line (one JSON line per point)")
     args = ap.parse_args(argv)
     if args.warmup < 3:

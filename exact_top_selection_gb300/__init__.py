@@ -24,7 +24,7 @@ from . import build as _build
 __all__ = [
     "DeviceInfo", "Plan", "PlanRequest", "ExactTopK", "ExactTopKError",
     "library", "library_path", "query_device", "make_plan", "workspace_size", "topk", "run",
-    "error_string", "version", "FAMILY_AUTO", "FAMILY_PERSISTENT_SAMPLED", "FAMILY_KV_SPLIT",
+    "error_string", "version", "stream_floor", "FAMILY_AUTO", "FAMILY_PERSISTENT_SAMPLED", "FAMILY_KV_SPLIT",
     "FAMILY_ROW_LOCAL_EXACT", "FAMILY_CLUSTER_SPLIT", "TRACE_FIELDS", "ROUTES", "EXPORTED_SYMBOLS",
 ]
 
@@ -41,7 +41,7 @@ TRACE_FIELDS = ("route", "tau0", "tau1", "c0", "c1", "tau_star", "e0", "q0")
 
 EXPORTED_SYMBOLS = ("exact_topk_query_device", "exact_topk_make_plan", "exact_topk_workspace_size",
                     "exact_topk", "exact_topk_run", "exact_topk_error_string",
-                    "exact_topk_version", "exact_topk_kv_split_noalloc")
+                    "exact_topk_version", "exact_topk_kv_split_noalloc", "exact_topk_stream_floor")
 
 
 class ExactTopKError(RuntimeError):
@@ -117,6 +117,8 @@ def library():
     lib.exact_topk_version.argtypes = []
     lib.exact_topk_kv_split_noalloc.argtypes = [p, c_i64, c_i64, p, p, p, c_int, p]
     lib.exact_topk_kv_split_noalloc.restype = c_int
+    lib.exact_topk_stream_floor.argtypes = [p, c_i64, c_i64, c_i64, p, p, c_int, p]
+    lib.exact_topk_stream_floor.restype = c_int
     for name in ("exact_topk_query_device", "exact_topk_make_plan", "exact_topk_workspace_size",
                  "exact_topk", "exact_topk_run", "exact_topk_version"):
         getattr(lib, name).restype = c_int
@@ -248,6 +250,26 @@ def run(plan: Plan, logits, ke, out, num_valid_rows, counters, workspace, prev_t
                                       0 if workspace is None else workspace.numel(),
                                       _ptr(prev_topk), _ptr(trace), _stream_handle(stream, dev))
     _check(rc, "exact_topk_run")
+    return out
+
+
+def stream_floor(logits, ke, splits, out=None, stream=None):
+    """Enqueues the streaming-floor kernel (reads each row's valid prefix
+    once, in `splits` segments per row); returns the [rows, splits] uint32
+    checksums.  A measurement utility, not a selection."""
+    import torch
+    dev = logits.device
+    _check_tensor(logits, "logits", torch.float32, dev, 2)
+    if logits.stride(1) != 1:
+        raise ValueError("logits rows must be contiguous")
+    M, N = logits.shape
+    _check_tensor(ke, "ke", torch.int32, dev, 1)
+    if out is None:
+        out = torch.empty(M, int(splits), dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        rc = library().exact_topk_stream_floor(_ptr(logits), M, N, logits.stride(0), _ptr(ke),
+                                               _ptr(out), int(splits), _stream_handle(stream, dev))
+    _check(rc, "exact_topk_stream_floor")
     return out
 
 

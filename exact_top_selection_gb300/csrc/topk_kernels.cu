@@ -3087,6 +3087,63 @@ __global__ void __launch_bounds__(kClusterThreads, 2) cluster_split_kernel(Param
   if (tid == 0 && cs.timed_out) flag_status(p.counters, 4);
 }
 
+// ----------------------------------------------------------------------------
+// Streaming floor (measurement)
+// ----------------------------------------------------------------------------
+
+// Reads the valid prefix of every live row exactly once (P CTAs per row, the
+// segments of segment_bounds, 256-bit loads with four in flight per thread)
+// and writes one checksum word per CTA: the time a kernel needs to read a
+// workload's algorithmic bytes in this launch shape, with nothing else to do.
+constexpr int kFloorThreads = 512;
+
+__global__ void __launch_bounds__(kFloorThreads) stream_floor_kernel(const float* logits,
+                                                                     int64_t pitch, int N,
+                                                                     int M_cap, const int32_t* ke,
+                                                                     uint32_t* out) {
+  const int r = blockIdx.y, P = gridDim.x, q = blockIdx.x;
+  if (r >= M_cap) return;
+  int L = ke[r];
+  L = L < 0 ? 0 : (L > N ? N : L);
+  int lo, hi;
+  segment_bounds(L, P, q, lo, hi);
+  const float* row = logits + (int64_t)r * pitch;
+  uint32_t acc = 0u;
+  if (lo < hi) {
+    const Span sp = aligned_span(row, lo, hi);
+    const int tid = threadIdx.x;
+    const int head = sp.a0 - lo, tail = hi - sp.a_end;
+    if (tid < head + tail) acc ^= ld_stream1(row + (tid < head ? lo + tid : sp.a_end + (tid - head)));
+    const float* body = row + sp.a0;
+    for (int v0 = 0; v0 < sp.nvec; v0 += 4 * kFloorThreads) {
+      uint32_t x[4][8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int v = v0 + k * kFloorThreads + tid;
+        if (v < sp.nvec) {
+          ld_stream8(body + 8 * v, x[k]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[k][e] = 0u;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc ^= x[k][e];
+    }
+  }
+  acc = __reduce_xor_sync(kFull, acc);
+  __shared__ uint32_t wx[kFloorThreads / 32];
+  if ((threadIdx.x & 31) == 0) wx[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t t = 0u;
+    for (int w = 0; w < kFloorThreads / 32; ++w) t ^= wx[w];
+    out[(int64_t)r * P + q] = t;
+  }
+}
+
 // Kernel attributes are set once per (device, kernel); later launches, which
 // may be inside a stream capture, only launch.
 constexpr int kMaxDevices = 64;
@@ -3370,4 +3427,23 @@ extern "C" int exact_topk_kv_split_noalloc(const float* logits, int64_t num_rows
   return exact_topk_run(&plan, logits, ke, out, num_valid_rows, scratch,
                         (size_t)plan.counter_bytes, scratch + ctr_bytes,
                         (size_t)plan.workspace_bytes, nullptr, nullptr, stream);
+}
+
+extern "C" int exact_topk_stream_floor(const float* logits, int64_t num_rows, int64_t max_kv_len,
+                                       int64_t row_pitch, const int32_t* ke, uint32_t* out,
+                                       int splits, struct CUstream_st* stream) {
+  using namespace etk;
+  if (logits == nullptr || ke == nullptr || out == nullptr) return EXACT_TOPK_ERR_NULL_POINTER;
+  if (num_rows < 1 || num_rows > 65535 || max_kv_len < 1 || max_kv_len > EXACT_TOPK_MAX_N ||
+      row_pitch < max_kv_len)
+    return EXACT_TOPK_ERR_BAD_SHAPE;
+  if (splits < 1 || splits > 1024) return EXACT_TOPK_ERR_BAD_PLAN;
+  if ((reinterpret_cast<uintptr_t>(logits) & 3u) != 0u ||
+      (reinterpret_cast<uintptr_t>(ke) & 3u) != 0u ||
+      (reinterpret_cast<uintptr_t>(out) & 3u) != 0u)
+    return EXACT_TOPK_ERR_MISALIGNED;
+  const dim3 grid((unsigned)splits, (unsigned)num_rows);
+  stream_floor_kernel<<<grid, kFloorThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      logits, row_pitch, (int)max_kv_len, (int)num_rows, ke, out);
+  return cudaGetLastError() == cudaSuccess ? EXACT_TOPK_OK : EXACT_TOPK_ERR_CUDA;
 }

@@ -244,6 +244,20 @@ int exact_topk_kv_split_noalloc(const float* logits, int64_t num_rows, int64_t m
                                 const int32_t* ke, int32_t* out, const int32_t* num_valid_rows,
                                 int top_k, struct CUstream_st* stream);
 
+/* Measurement utility, not part of the selection: reads the valid prefix
+ * [0, clamp(ke[r], 0, max_kv_len)) of every row r < num_rows exactly once,
+ * split into `splits` contiguous segments per row (one 512-thread CTA each,
+ * 256-bit loads), and writes an XOR checksum of each segment's bit patterns
+ * to out[r * splits + p] (device uint32 [num_rows][splits]).  Its duration is
+ * the streaming floor of a workload: the time to read the algorithmic score
+ * bytes of the roofline (section 6.1's complete-row work) in a comparable
+ * launch shape, with no selection work.  Enqueues one kernel on `stream`.
+ * Errors: ERR_NULL_POINTER, ERR_BAD_SHAPE, ERR_BAD_PLAN (splits outside
+ * [1, 1024]), ERR_MISALIGNED (4-byte alignment), ERR_CUDA. */
+int exact_topk_stream_floor(const float* logits, int64_t num_rows, int64_t max_kv_len,
+                            int64_t row_pitch, const int32_t* ke, uint32_t* out, int splits,
+                            struct CUstream_st* stream);
+
 /* Static description of a status code; never NULL. */
 const char* exact_topk_error_string(int status);
 

@@ -472,3 +472,25 @@ def test_cluster_split_wide_forced_routes(dual):
         assert tr[:, 0].tolist() == [1, 2, 3, 5]
     else:
         assert tr[:3, 0].tolist() == [1, 4, 4]
+
+
+@pytest.mark.parametrize("splits", [1, 4, 7])
+def test_stream_floor_reads_exactly_the_valid_prefixes(splits):
+    # The streaming-floor kernel (a measurement utility): its per-segment
+    # checksums equal XORs over the segments of each row's valid prefix.
+    M, N = 5, 70001
+    rng = np.random.default_rng(splits)
+    X = rng.standard_normal((M, N)).astype(np.float32)
+    ke = np.array([N, 0, 1, 33333, N + 9], np.int32)
+    dev = torch.device("cuda")
+    out = etk.stream_floor(torch.as_tensor(X).to(dev), torch.as_tensor(ke).to(dev), splits)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().view(np.uint32)
+    bits = X.view(np.uint32)
+    for r in range(M):
+        L = int(min(max(int(ke[r]), 0), N))
+        seg = ((L + splits - 1) // splits + 7) // 8 * 8
+        for q in range(splits):
+            lo, hi = min(L, q * seg), min(L, q * seg + seg)
+            exp = np.bitwise_xor.reduce(bits[r, lo:hi]) if hi > lo else np.uint32(0)
+            assert got[r, q] == exp, (r, q)
