@@ -14,10 +14,13 @@ namespace etk {
 // Counter buffer layout (int32 words).  The queue head and exit counter drive
 // the persistent row queue; arrive[r] elects the KV-split finisher of row r;
 // status is a sticky error word that stays zero unless a device-side bounds
-// guard tripped.  Every launch returns words 0, 1 and arrive[] to zero.
+// guard tripped; the deferred count hands rows from the persistent kernel to
+// the heavy-row kernel that follows it.  Every call returns words 0, 1, 3 and
+// arrive[] to zero.
 constexpr int kCtrQueue = 0;
 constexpr int kCtrExit = 1;
 constexpr int kCtrStatus = 2;
+constexpr int kCtrDeferred = 3;  // persistent family: rows handed to the heavy-row kernel
 constexpr int kCtrArriveBase = 4;
 
 #ifndef ETK_PERSISTENT_THREADS
@@ -63,6 +66,7 @@ size_t shared_bytes(int family, int cap);
 struct WorkspaceLayout {
   uint64_t pair_offset;   // (int32 index, uint32 key) pairs [slices][N]
   uint64_t seg_offset;    // int32 pairs [M][P] (KV-split published counts)
+  uint64_t defer_offset;  // persistent family: int32 [M][8] deferred-row records
   uint64_t total;
   int64_t slices;
 };

@@ -76,6 +76,9 @@ WorkspaceLayout workspace_layout(const exact_topk_plan& plan) {
   lay.seg_offset = off;
   if (plan.family == EXACT_TOPK_FAMILY_KV_SPLIT)
     off = round_up(off + (uint64_t)plan.num_rows * (uint64_t)plan.splits * 8u, kAlign);
+  lay.defer_offset = off;
+  if (plan.family == EXACT_TOPK_FAMILY_PERSISTENT_SAMPLED)
+    off = round_up(off + (uint64_t)plan.num_rows * 32u, kAlign);
   lay.total = off;
   return lay;
 }

@@ -301,7 +301,8 @@ struct Slot {
   int32_t c0, c1, tstar, e0, q0n;
   uint32_t seg_c0, seg_cb;  // KV-split: this segment's counts
   int32_t is_last;
-  int32_t pad_[3];
+  uint32_t vcnt0;  // Phase 1: view entries in bins <= tau0
+  int32_t pad_[2];
 };
 
 struct Params {
@@ -323,6 +324,7 @@ struct Params {
   int32_t* counters;
   uint2* ws;            // [slices][N] (index, key) pairs
   int32_t* seg_counts;  // [M_cap][P][2]
+  int32_t* defer;       // persistent family: [M_cap][8] deferred-row records
   const int32_t* prev;
   int32_t* trace;
   // Persistent kernel: tiled tensor map over the scores seen as
@@ -384,6 +386,10 @@ constexpr int kRefineWarps = kPersistentThreads / 32 - ETK_PREPARE_WARPS;
 static_assert(kRefineWarps > 0 && kRefineWarps < kPersistentThreads / 32,
               "both groups need at least one warp");
 
+// Rows one persistent CTA may hand to its own epilogue (heavy rows beyond
+// these take the frontier route).
+constexpr uint32_t kMaxOwnDeferred = 63;
+
 // Dynamic shared memory layouts (byte offsets), one per kernel family.
 struct SmemLayout {
   uint32_t slots;     // Slot[nslots]
@@ -393,6 +399,7 @@ struct SmemLayout {
   uint32_t runs;      // KV-split run table, or 0
   uint32_t vbuf;      // persistent: TMA view boxes, kViewBoxes x 4 KB (128-byte aligned), or 0
   uint32_t vbar;      // persistent: the view copies' mbarrier, and its phase word, or 0
+  uint32_t own;       // persistent: count and indices of the rows this CTA deferred, or 0
   uint32_t queues;    // uint32[warps][kQueueWords]
   uint32_t total;
 };
@@ -428,6 +435,8 @@ __host__ __device__ constexpr SmemLayout smem_layout(int family, int cap) {
     o += kViewBoxes * 4096u;
     l.vbar = o;
     o = align16(o + 16u);
+    l.own = o;
+    o = align16(o + (1u + kMaxOwnDeferred) * 4u);
   }
   l.queues = o;
   o = align16(o + qwarps * kQueueWords * 4u);
@@ -1369,6 +1378,166 @@ __device__ void refine(const Frontier& F, uint32_t n, uint32_t k, uint32_t* hist
 }
 
 // ----------------------------------------------------------------------------
+// Phase 3 over the row itself (frontiers too large to hold)
+// ----------------------------------------------------------------------------
+
+// Over the keys d <= T in [qlo, qhi) of row[0, L), by group G: the histogram
+// of their digits (d - qlo) >> shift (when `hist` is not null), and each
+// thread's count, smallest and largest key (accumulated into cnt, mn, mx).
+// Four 256-bit loads per thread in flight, run-length merged adds.  No group
+// barrier.
+template <class G>
+__device__ void scan_key_hist(const float* row, int L, uint32_t T, uint64_t qlo, uint64_t qhi,
+                              int shift, uint32_t* hist, uint32_t& cnt, uint32_t& mn,
+                              uint32_t& mx) {
+  const int tid = G::rank();
+  const Span sp = aligned_span(row, 0, L);
+  auto take = [&](uint32_t d) {
+    if (d <= T && (uint64_t)d >= qlo && (uint64_t)d < qhi) {
+      ++cnt;
+      mn = min(mn, d);
+      mx = max(mx, d);
+      return true;
+    }
+    return false;
+  };
+  const int head = sp.a0, tail = L - sp.a_end;
+  if (tid < head + tail) {
+    const uint32_t d = desc_key(ld_stream1(row + (tid < head ? tid : sp.a_end + (tid - head))));
+    if (take(d) && hist != nullptr) smem_add(&hist[(uint32_t)(((uint64_t)d - qlo) >> shift)], 1u);
+  }
+  const float* body = row + sp.a0;
+  constexpr int kV = 2;
+  for (int t0 = 0; t0 < sp.nvec; t0 += kV * G::kThreads) {
+    uint32_t x[kV][8];
+#pragma unroll
+    for (int k = 0; k < kV; ++k) {
+      const int v = t0 + k * G::kThreads + tid;
+      if (v < sp.nvec) {
+        ld_stream8(body + 8 * v, x[k]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[k][e] = 0xFFFFFFFFu;
+      }
+    }
+    RunHist rh;
+#pragma unroll
+    for (int k = 0; k < kV; ++k) {
+      if (t0 + k * G::kThreads + tid >= sp.nvec) break;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const uint32_t d = desc_key(x[k][e]);
+        if (take(d) && hist != nullptr) rh.add(hist, (uint32_t)(((uint64_t)d - qlo) >> shift));
+      }
+    }
+    if (hist != nullptr) rh.flush(hist);
+  }
+}
+
+// Commit pass over row[0, L) by group G: every key d <= T below commit_below
+// goes to the output, then the first `ties` keys equal to tie_key (ranked
+// through sl.n_keep).  Per thread and 8-score vector, the committed and tied
+// positions are bit masks; one warp scan ranks the ties and one places the
+// outputs, so a warp issues two atomics per vector step whatever it commits.
+// Ends with a group barrier.
+template <class G>
+__device__ void scan_commit(const float* row, int L, uint32_t T, uint64_t commit_below,
+                            uint32_t tie_key, uint32_t ties, Slot& sl, int32_t* out_row, int K) {
+  const int tid = G::rank(), lane = tid & 31;
+  if (tid == 0) sl.n_keep = 0u;
+  G::sync();
+  auto warp_excl = [&](uint32_t v, uint32_t& total) {
+    uint32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += y;
+    }
+    total = __shfl_sync(kFull, incl, 31);
+    return incl - v;
+  };
+  // whole warps: x[0..8) with positions i0 .. i0+7, valid below `nvalid`
+  auto step = [&](const uint32_t* x, int i0, int nvalid) {
+    uint32_t cm = 0u, tm = 0u;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const uint32_t d = desc_key(x[e]);
+      const bool ok = e < nvalid && d <= T;
+      if (ok && (uint64_t)d < commit_below)
+        cm |= 1u << e;
+      else if (ok && ties > 0u && d == tie_key)
+        tm |= 1u << e;
+    }
+    if (tm != 0u && *(volatile uint32_t*)&sl.n_keep >= ties) tm = 0u;  // ties complete
+    if (__ballot_sync(kFull, (cm | tm) != 0u) == 0u) return;
+    if (__ballot_sync(kFull, tm != 0u) != 0u) {
+      uint32_t tt;
+      const uint32_t tex = warp_excl((uint32_t)__popc(tm), tt);
+      uint32_t base = 0u;
+      if (lane == 0) base = atomicAdd(&sl.n_keep, tt);
+      base = __shfl_sync(kFull, base, 0);
+      // keep the ties ranked below `ties`
+      uint32_t rank = base + tex;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if (tm & (1u << e)) {
+          if (rank >= ties) tm &= ~(1u << e);
+          ++rank;
+        }
+      }
+    }
+    const uint32_t m = cm | tm;
+    uint32_t tot;
+    const uint32_t ex = warp_excl((uint32_t)__popc(m), tot);
+    uint32_t base = 0u;
+    if (lane == 0 && tot) base = atomicAdd(&sl.n_out, tot);
+    base = __shfl_sync(kFull, base, 0);
+    uint32_t slot = base + ex;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      if (m & (1u << e)) {
+        if (slot < (uint32_t)K) out_row[slot] = i0 + e;
+        ++slot;
+      }
+    }
+  };
+  const Span sp = aligned_span(row, 0, L);
+  const int head = sp.a0, tail = L - sp.a_end;
+  if (tid < 32) {  // the scalar head and tail (at most 14 scores), one lane each
+    uint32_t x[8];
+    const bool valid = tid < head + tail;
+    const int i = tid < head ? tid : sp.a_end + (tid - head);
+    x[0] = valid ? ld_stream1(row + i) : 0xFFFFFFFFu;
+#pragma unroll
+    for (int e = 1; e < 8; ++e) x[e] = 0xFFFFFFFFu;
+    step(x, i, valid ? 1 : 0);
+  }
+  const float* body = row + sp.a0;
+  constexpr int kV = 2;  // vectors per thread in flight
+  const int nvr = (sp.nvec + 31) & ~31;
+  for (int t0 = 0; t0 < nvr; t0 += kV * G::kThreads) {
+    uint32_t x[kV][8];
+#pragma unroll
+    for (int k = 0; k < kV; ++k) {
+      const int v = t0 + k * G::kThreads + tid;
+      if (v < sp.nvec) {
+        ld_stream8(body + 8 * v, x[k]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[k][e] = 0xFFFFFFFFu;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kV; ++k) {
+      const int v = t0 + k * G::kThreads + tid;
+      if (t0 + k * G::kThreads + 32 * (tid >> 5) >= nvr) break;  // warp-uniform
+      step(x[k], sp.a0 + 8 * v, v < sp.nvec ? 8 : 0);
+    }
+  }
+  G::sync();
+}
+
+// ----------------------------------------------------------------------------
 // Row-level building blocks
 // ----------------------------------------------------------------------------
 
@@ -1563,6 +1732,7 @@ __device__ void view_cutoffs(const Params& p, const uint32_t* hist, GroupScratch
       if (warp == 0) {
         sl.T0 = t;
         sl.tau0 = b;
+        sl.vcnt0 = b >= 0 ? sc.res_below[0] + sc.res_cnt[0] : 0u;
       } else {
         sl.T1 = t;
         sl.tau1 = b;
@@ -1671,6 +1841,7 @@ __device__ void exit_protocol(int32_t* counters) {
     if (prev == (int)(gridDim.x * gridDim.y) - 1) {
       atomicExch(counters + kCtrQueue, 0);
       atomicExch(counters + kCtrExit, 0);
+      atomicExch(counters + kCtrDeferred, 0);
     }
   }
 }
@@ -1834,6 +2005,14 @@ constexpr int kNextPad = 0;      // L <= K: padded output, no selection
 constexpr int kNextSampled = 1;  // view cutoffs T0 (and T1) in the slot
 constexpr int kNextDirect = 2;   // view too small: exact coarse recovery
 constexpr int kNextGuess = 3;    // guess-source cutoff T0 in the slot
+constexpr int kNextDeferred = 4; // handed to the heavy-row kernel (record in Params::defer)
+
+// A sampled row whose view predicts C(tau0) ~ s * (view entries in bins <=
+// tau0) above eight on-chip frontier capacities: a tie group or a constant
+// row admitted whole.
+__device__ __forceinline__ bool heavy_view(const Params& p, const Slot& nx) {
+  return p.defer != nullptr && (uint64_t)nx.vcnt0 * (uint64_t)p.s > 8ull * (uint64_t)p.cap;
+}
 
 // Claims a row (or takes `assigned`) and runs its Phase 1 by group V into
 // `nx`, with `vh` as the view histogram.  The caller publishes `nx` with a CTA
@@ -1877,6 +2056,27 @@ __device__ void prepare_row(const Params& p, int M, int assigned, Slot& nx, uint
         else
           sample_view<V>(p, row, L, a, vh, sc, nx);
         kind = kNextSampled;
+        // this CTA's list of deferred rows (persistent layout)
+        uint32_t* own = reinterpret_cast<uint32_t*>(
+            smem_base() + smem_layout(EXACT_TOPK_FAMILY_PERSISTENT_SAMPLED, kPersistentCap).own);
+        if (heavy_view(p, nx) && own[0] < kMaxOwnDeferred) {
+          // the rest of this row's method runs in the CTA's epilogue
+          // (finish_deferred), after its other rows
+          V::sync();  // every thread has read own[0]
+          if (V::rank() == 0) {
+            const int i = atomicAdd(p.counters + kCtrDeferred, 1);
+            int32_t* rec = p.defer + 8 * (int64_t)i;
+            rec[0] = nr;
+            rec[1] = L;
+            rec[2] = (int32_t)nx.T0;
+            rec[3] = (int32_t)nx.T1;
+            rec[4] = nx.tau0;
+            rec[5] = nx.tau1;
+            own[1 + own[0]] = (uint32_t)i;
+            own[0] = own[0] + 1u;
+          }
+          kind = kNextDeferred;
+        }
       } else {
         kind = kNextDirect;
       }
@@ -1904,7 +2104,8 @@ __device__ void persistent_row(const Params& p, int M, Slot& sl, Slot& nx, const
   const int tau0 = nx.tau0, tau1 = nx.tau1;
   const float* row = p.logits + (int64_t)r * p.pitch;
   int32_t* out_row = p.out + (int64_t)r * K;
-  if (kind != kNextPad) clear_hist<G>(hist, 2048);
+  const bool idle = kind == kNextPad || kind == kNextDeferred;  // no selection work here
+  if (!idle) clear_hist<G>(hist, 2048);
   if (threadIdx.x == 0) {
     sl.row = r;
     sl.L = L;
@@ -1924,6 +2125,8 @@ __device__ void persistent_row(const Params& p, int M, Slot& sl, Slot& nx, const
   if (kind == kNextPad) {
     write_pad_row<G>(out_row, L, K);
     if (threadIdx.x == 0) write_trace(p, r, EXACT_TOPK_ROUTE_PAD, -1, -1, -1, -1, -1, -1, -1);
+  } else if (kind == kNextDeferred) {
+    // written by the heavy-row kernel
   } else {
     FrontierSink front_sink{{}, F, hist};
     DropSink drop;
@@ -1973,7 +2176,7 @@ __device__ void persistent_row(const Params& p, int M, Slot& sl, Slot& nx, const
   // frontier is in shared memory; one after the other, each by the whole CTA,
   // when it spilled (refinement then streams the global slice and wants every
   // warp) or when there is nothing to refine.
-  const bool split = kind != kNextPad && sl.n_front <= F.cap;
+  const bool split = !idle && sl.n_front <= F.cap;
   if (split) {
     if ((int)(threadIdx.x >> 5) < kRefineWarps) {
       refine<R>(F, sl.n_front, (uint32_t)(K - sl.e0), hist, sc, sl, out_row, K, queues,
@@ -1984,7 +2187,7 @@ __device__ void persistent_row(const Params& p, int M, Slot& sl, Slot& nx, const
       prepare_row<V>(p, M, -1, nx, vhist, sc2[1], vd);
     }
   } else {
-    if (kind != kNextPad) {
+    if (!idle) {
       refine<G>(F, sl.n_front, (uint32_t)(K - sl.e0), hist, sc, sl, out_row, K, queues,
                 (uint32_t)(G::kWarps * kQueueWords));
       finish_row<G>(p, sl, out_row);
@@ -1994,6 +2197,9 @@ __device__ void persistent_row(const Params& p, int M, Slot& sl, Slot& nx, const
   }
   __syncthreads();
 }
+
+// Finishes the rows this CTA deferred (defined with the heavy-row machinery).
+__device__ __noinline__ void finish_deferred(const Params& p);
 
 __global__ void __launch_bounds__(kPersistentThreads, 1024 / kPersistentThreads)
     persistent_sampled_kernel(const __grid_constant__ Params p) {
@@ -2014,12 +2220,14 @@ __global__ void __launch_bounds__(kPersistentThreads, 1024 / kPersistentThreads)
       // the boxes' shared destination must be 128-byte aligned: otherwise the
       // buffer is retired from the start and the view is gathered directly
       *vd.phase = (smem_addr(vd.buf) & 127u) == 0u ? 0u : 2u;
+      *reinterpret_cast<uint32_t*>(sm + lay.own) = 0u;
     }
     __syncthreads();
     prepare_row<CtaGroup<kPersistentThreads>>(p, M, (int)blockIdx.x, slots[1], vhist, sc2[1], vd);
     __syncthreads();
     while (slots[1].route != kNextNone)
       persistent_row(p, M, slots[0], slots[1], F, hist, vhist, sc2, queues, vd);
+    if (*reinterpret_cast<const uint32_t*>(smem_base() + lay.own) != 0u) finish_deferred(p);
   }
   exit_protocol(p.counters);
 }
@@ -3144,6 +3352,164 @@ __global__ void __launch_bounds__(kFloorThreads) stream_floor_kernel(const float
   }
 }
 
+// ----------------------------------------------------------------------------
+// Heavy rows of the persistent kernel
+// ----------------------------------------------------------------------------
+//
+// Rows whose Phase 1 predicts a frontier far beyond on-chip capacity (a tie
+// group or a constant row admitted whole, the |Q0| = L worst case of section
+// 4.4) are set aside by the persistent CTA that claimed them and finished in
+// its epilogue, after its other rows, without materializing the frontier: the
+// counts of eqs. 16-19, the exact coarse recovery of eq. 20 when they fall
+// short, and the digit rounds of eqs. 22-25 all run as histogram passes over
+// the row itself, and one final pass commits the keys below the threshold and
+// the first ties (eq. 25).  The routes and trace fields are those of the
+// frontier method.
+
+// Count, smallest and largest of the keys d <= T in [qlo, qhi) of the row,
+// and (hist not null) their digit histogram from a clear one; block-wide
+// results, valid for every thread on return.
+template <class G>
+__device__ void row_pass(const float* row, int L, uint32_t T, uint64_t qlo, uint64_t qhi,
+                         int shift, int nbins, uint32_t* hist, GroupScratch& sc, uint32_t& cnt,
+                         uint32_t& kmin, uint32_t& kmax) {
+  G::sync();  // hist and the scratch are free
+  if (hist != nullptr) clear_hist<G>(hist, nbins);
+  if (G::rank() == 0) sc.bcast = 0;
+  G::sync();
+  uint32_t c = 0u, mn = 0xFFFFFFFFu, mx = 0u;
+  scan_key_hist<G>(row, L, T, qlo, qhi, shift, hist, c, mn, mx);
+  c = __reduce_add_sync(kFull, c);
+  if ((G::rank() & 31) == 0 && c) atomicAdd(&sc.bcast, (int)c);
+  block_min_max<G>(mn, mx, sc, kmin, kmax);  // ends with a group barrier
+  cnt = (uint32_t)sc.bcast;
+}
+
+// The k smallest keys among the keys d <= T of the row, all in [kmin, kmax]:
+// each round histograms an 11-bit digit over the interval left in play,
+// narrows it to the bucket holding the k-th key, and in the same pass
+// measures the range of the keys in play, so that a range of one value ends
+// the rounds with k ties (eq. 25).  The threshold is the one eqs. 22-25 reach.
+template <class G>
+__device__ Cut row_radix(const float* row, int L, uint32_t T, uint32_t k, uint32_t kmin,
+                         uint32_t kmax, uint32_t* hist, GroupScratch& sc) {
+  Cut cut{0, 0u, 0u, false};
+  uint64_t qlo = kmin, qhi = (uint64_t)kmax + 1u;  // keys in play
+  for (int round = 0; round < 6; ++round) {
+    if (kmin > kmax) break;  // nothing in play: inconsistent counts
+    if (kmin == kmax) {
+      cut.commit_below = kmin;  // every key in play equal: k ties
+      cut.tie_key = kmin;
+      cut.ties = k;
+      return cut;
+    }
+    // the measured range narrows the interval
+    if ((uint64_t)kmin > qlo) qlo = kmin;
+    if ((uint64_t)kmax + 1u < qhi) qhi = (uint64_t)kmax + 1u;
+    const int bits = 64 - __clzll((long long)(qhi - qlo - 1u));
+    const int shift = bits > 11 ? bits - 11 : 0;
+    const int nbins = (int)((((qhi - qlo - 1u) >> shift) + 1u + 127u) & ~127ull);
+    uint32_t c;
+    row_pass<G>(row, L, T, qlo, qhi, shift, nbins, hist, sc, c, kmin, kmax);
+    if (kmin == kmax) continue;  // one value left: ties (top of the loop)
+    find_boundaries<G>(hist, sc, nbins, 1, k, 0u);
+    const int b = sc.res_bin[0];
+    const uint32_t below = sc.res_below[0], cnt = sc.res_cnt[0];
+    if (b < 0) break;
+    qlo += (uint64_t)b << shift;
+    const uint64_t top = qlo + ((uint64_t)1 << shift);
+    qhi = top < qhi ? top : qhi;
+    if (below + cnt == k) {
+      cut.commit_below = qhi;  // the bucket closes the quota
+      return cut;
+    }
+    k -= below;
+    // the bucket's range is measured by the next round's pass
+    kmin = (uint32_t)qlo;
+    kmax = (uint32_t)(qhi - 1u);
+    if (qhi - qlo == 1u) continue;
+  }
+  cut.bad = true;
+  return cut;
+}
+
+template <class G>
+__device__ void heavy_row(const Params& p, const int32_t* rec, uint32_t* hist, GroupScratch& sc,
+                          Slot& sl) {
+  const int r = rec[0], L = rec[1];
+  const uint32_t T0 = (uint32_t)rec[2], T1 = (uint32_t)rec[3];
+  const int tau0 = rec[4], tau1 = rec[5];
+  const int K = p.K;
+  const float* row = p.logits + (int64_t)r * p.pitch;
+  int32_t* out_row = p.out + (int64_t)r * K;
+  if (G::rank() == 0) {
+    sl.n_out = 0u;
+    sl.n_keep = 0u;
+  }
+  // Phase 2 counts (eqs. 16-19) with the range of the admitted keys
+  uint32_t c0, kmin, kmax;
+  row_pass<G>(row, L, T0, 0u, (uint64_t)T0 + 1u, 0, 0, nullptr, sc, c0, kmin, kmax);
+  int route, c1 = -1, tstar = -1, e0 = 0, q0;
+  uint32_t T = T0;
+  bool ok = true;
+  if (c0 >= (uint32_t)K) {
+    route = EXACT_TOPK_ROUTE_PRIMARY;
+    q0 = (int)c0;
+  } else {
+    route = EXACT_TOPK_ROUTE_EXACT_NO_BAND;
+    q0 = 0;
+    if (p.dual) {
+      uint32_t cb;
+      row_pass<G>(row, L, T1, 0u, (uint64_t)T1 + 1u, 0, 0, nullptr, sc, cb, kmin, kmax);
+      c1 = (int)cb;  // band rescue: C(tau1)
+      route = c1 >= K ? EXACT_TOPK_ROUTE_BAND : EXACT_TOPK_ROUTE_EXACT_AFTER_BAND;
+      T = T1;
+      q0 = c1;
+    }
+    if (route != EXACT_TOPK_ROUTE_BAND) {
+      // exact coarse recovery (eq. 20): tau* = min{b : C(b) >= K}; the keys of
+      // bins below tau* (E0) are committed by the final pass, Q0 = bin tau*
+      G::sync();
+      clear_hist<G>(hist, 2048);
+      G::sync();
+      scan_coarse_hist<G>(row, 0, L, hist);
+      G::sync();
+      find_boundaries<G>(hist, sc, 2048, 1, (uint32_t)K, 0u);
+      tstar = sc.res_bin[0];
+      e0 = (int)sc.res_below[0];
+      q0 = (int)sc.res_cnt[0];
+      ok = tstar >= 0;
+      exact_cutoffs<G>(sl, ok ? tstar : 0);
+      T = sl.T1;
+      const uint32_t lo = tstar > 0 ? sl.T0 + 1u : 0u;
+      uint32_t cq;
+      row_pass<G>(row, L, T, lo, (uint64_t)T + 1u, 0, 0, nullptr, sc, cq, kmin, kmax);
+    }
+  }
+  Cut cut{0, 0u, 0u, true};
+  if (ok) cut = row_radix<G>(row, L, T, (uint32_t)(K - e0), kmin, kmax, hist, sc);
+  if (!cut.bad) scan_commit<G>(row, L, T, cut.commit_below, cut.tie_key, cut.ties, sl, out_row, K);
+  finish_row<G>(p, sl, out_row);
+  if (G::rank() == 0) write_trace(p, r, route, tau0, tau1, (int)c0, c1, tstar, e0, q0);
+}
+
+// Out of line, with its shared-memory views rebuilt here: nothing of the
+// epilogue stays live through the row loop.
+__device__ __noinline__ void finish_deferred(const Params& p) {
+  using G = CtaGroup<kPersistentThreads>;
+  unsigned char* sm = smem_base();
+  constexpr SmemLayout lay = smem_layout(EXACT_TOPK_FAMILY_PERSISTENT_SAMPLED, kPersistentCap);
+  const uint32_t* own = reinterpret_cast<const uint32_t*>(sm + lay.own);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(sm + lay.hist);
+  GroupScratch& sc = *reinterpret_cast<GroupScratch*>(sm + lay.scratch);
+  Slot& sl = *reinterpret_cast<Slot*>(sm + lay.slots);
+  const uint32_t n = own[0];
+  for (uint32_t j = 0; j < n; ++j) {
+    heavy_row<G>(p, p.defer + 8 * (int64_t)own[1 + j], hist, sc, sl);
+    __syncthreads();
+  }
+}
+
 // Kernel attributes are set once per (device, kernel); later launches, which
 // may be inside a stream capture, only launch.
 constexpr int kMaxDevices = 64;
@@ -3285,6 +3651,9 @@ int launch(const exact_topk_plan& plan, const LaunchArgs& a, cudaStream_t stream
   p.seg_counts = plan.family == EXACT_TOPK_FAMILY_KV_SPLIT
                      ? reinterpret_cast<int32_t*>(ws + lay.seg_offset)
                      : nullptr;
+  p.defer = plan.family == EXACT_TOPK_FAMILY_PERSISTENT_SAMPLED && ws != nullptr
+                ? reinterpret_cast<int32_t*>(ws + lay.defer_offset)
+                : nullptr;
   p.prev = a.prev_topk;
   p.trace = a.trace;
   p.view_tma = 0;
@@ -3298,6 +3667,9 @@ int launch(const exact_topk_plan& plan, const LaunchArgs& a, cudaStream_t stream
       rc = set_attrs(persistent_sampled_kernel, EXACT_TOPK_FAMILY_PERSISTENT_SAMPLED, smem);
       if (rc != EXACT_TOPK_OK) return rc;
       persistent_sampled_kernel<<<plan.workers, kPersistentThreads, smem, stream>>>(p);
+      // rows the persistent kernel deferred (predicted frontiers far beyond
+      // on-chip capacity); exits at once when there are none
+
       break;
     case EXACT_TOPK_FAMILY_KV_SPLIT: {
       if (plan.splits > kMaxSplits) return EXACT_TOPK_ERR_BAD_PLAN;

@@ -77,6 +77,9 @@ def test_planner_families(M, N, K, family, stride, dual):
     elif N > p.cand_capacity:
         assert p.workers == min(M, 152 * (3 if family == 1 else 1))
         assert p.workspace_bytes >= p.workers * N * 8
+    elif family == etk.FAMILY_PERSISTENT_SAMPLED:
+        # no frontier slices; one 32-byte record per row for deferred rows
+        assert p.workspace_bytes == -(-M * 32 // 256) * 256
     else:
         assert p.workspace_bytes == 0
 

@@ -494,3 +494,38 @@ def test_stream_floor_reads_exactly_the_valid_prefixes(splits):
             lo, hi = min(L, q * seg), min(L, q * seg + seg)
             exp = np.bitwise_xor.reduce(bits[r, lo:hi]) if hi > lo else np.uint32(0)
             assert got[r, q] == exp, (r, q)
+
+
+@pytest.mark.parametrize("workers", [1, 3, 0])
+def test_persistent_heavy_rows_deferred_and_overflowing(workers):
+    # Rows whose view predicts a frontier far beyond on-chip capacity
+    # (constant, -inf, signed-zero, two-level and subnormal rows) are finished
+    # after the CTA's other rows, by passes over the row itself; on one worker
+    # more than its 63-entry list of such rows exist, and the rest take the
+    # frontier route.  Mixed with ordinary, padded and empty rows.
+    M, N, K = 90, 40000, 512
+    rng = np.random.default_rng(4242)
+    X = rng.standard_normal((M, N)).astype(np.float32)
+    ke = rng.integers(K + 1, N + 1, M).astype(np.int32)
+    for r in range(M):
+        kind = r % 6
+        if kind == 0:
+            X[r] = 0.75
+        elif kind == 1:
+            X[r] = -np.inf
+        elif kind == 2:
+            X[r] = np.where(rng.integers(0, 2, N) == 1, np.float32(-0.0), np.float32(0.0))
+        elif kind == 3:
+            X[r] = 0.0
+            X[r, rng.permutation(N)[:K + (r % 5) - 2]] = 1.0
+        elif kind == 4:  # subnormals of both signs: sign bit over a 23-bit mantissa
+            X[r] = (rng.integers(1, 1 << 23, N).astype(np.uint32) |
+                    (rng.integers(0, 2, N).astype(np.uint32) << np.uint32(31))).view(np.float32)
+    ke[5], ke[11], ke[17] = 0, K, 7
+    for r in range(M):
+        X[r, ke[r]:] = np.nan
+    out, tr, plan, ctr = run_gpu(X, ke, K, family=etk.FAMILY_PERSISTENT_SAMPLED, workers=workers)
+    compare_rows(X, ke, K, out)
+    assert_counters_zero(ctr)
+    _, tr_ref = oracle_trace_for_plan(X, ke, K, plan)
+    compare_trace(tr, tr_ref)
