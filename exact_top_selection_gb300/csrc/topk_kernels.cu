@@ -47,13 +47,15 @@ namespace {
 
 constexpr int kCoarseBins = 2048;
 constexpr int kMaxSplits = 128;
-// Depth of each thread's ring of 256-bit loads in a complete-row pass.  Three
-// (two vectors in flight while one is filtered) measured faster than four in
-// the persistent kernel on GB300: at 64 registers a thread the fourth vector
-// makes the kernel spill, and the TMA L2 prefetch ahead of the pass already
-// keeps bytes in flight that hold no registers.
+// Depth of each thread's ring of 256-bit loads in a complete-row pass.  Two
+// (one vector in flight while one is filtered) is the fastest on GB300: the
+// persistent kernel runs at 64 registers a thread, every deeper slot holds
+// eight more of them live across the filter (the causal prefill batch,
+// 4096 rows of up to 131072 scores, takes 418 us at depth two, 434 us at
+// three), and the TMA L2 prefetch ahead of the pass already keeps bytes in
+// flight that hold no registers.
 #ifndef ETK_RING
-#define ETK_RING 3
+#define ETK_RING 2
 #endif
 constexpr int kRing = ETK_RING;
 constexpr uint32_t kDescPosInf = 0x007FFFFFu;  // kappa_down32(+inf)
