@@ -1631,6 +1631,74 @@ __device__ void exact_recovery(const Params& p, const float* row, int L, const F
   G::sync();
 }
 
+// Exact coarse recovery bounded by the view (sampled rows).  Phase 2 left
+// cb < K keys in the frontier, every key d <= Tb (the cutoff of bin tau_b),
+// so the K-th key lies in a later coarse bin.  The view's histogram predicts
+// how many keys the next bins hold: one pass appends Tb < d <= T2, T2 the
+// cutoff of the first bin b2 (at most 32 bins on) whose predicted addition
+// covers twice the shortfall plus two view strides.  When the frontier then
+// holds K keys or more, it holds every key of the bins up to b2, so its
+// coarse histogram gives tau*, |E0| and |Q0| of eq. 20 exactly, and it holds
+// the whole Top-K: Phase 3 refines it with k = K and nothing committed.  The
+// result is that of the full-row recovery with one pass over the row instead
+// of two (a full-row coarse histogram is one shared-memory add per score).
+// Returns false when no bin qualifies or the count still falls short; the
+// caller then runs the full-row recovery.  `view` holds the row's view
+// histogram on entry and the frontier's coarse histogram on a true return.
+template <class G>
+__device__ bool bounded_recovery(const Params& p, const float* row, int L, const Frontier& F,
+                                 uint32_t* hist, uint32_t* view, GroupScratch& sc, Slot& sl,
+                                 uint32_t* queues, uint32_t Tb, int tau_b) {
+  const uint32_t K = (uint32_t)p.K;
+  if (G::rank() < 32) {
+    const int lane = G::rank();
+    const int b = tau_b + 1 + lane;
+    uint32_t v = b < kCoarseBins ? view[b] : 0u;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t t = __shfl_up_sync(kFull, v, o);
+      if (lane >= o) v += t;
+    }
+    const uint64_t need = 2ull * (K - sl.n_front) + 2ull * (uint32_t)p.s;
+    const unsigned m =
+        __ballot_sync(kFull, b < kCoarseBins && (uint64_t)v * (uint32_t)p.s >= need);
+    const int b2 = m != 0u ? tau_b + __ffs((int)m) : -1;  // first qualifying bin
+    uint32_t T2 = 0u;
+    if (b2 >= 0) T2 = cutoff_fast_warp(b2);
+    if (lane == 0) {
+      sc.bcast = b2;
+      sc.bcast2 = (int32_t)T2;
+    }
+  }
+  G::sync();
+  const int b2 = sc.bcast;
+  const uint32_t T2 = (uint32_t)sc.bcast2;
+  if (b2 < 0) return false;
+  FrontierSink front_sink{{}, F, hist};
+  DropSink drop;
+  scan_two_class<G>(row, 0, L, Tb, T2, true, &sl.n_drop, &sl.n_front, queues, drop, front_sink);
+  G::sync();
+  const uint32_t c2 = sl.n_front;
+  if (c2 < K) return false;
+  clear_hist<G>(view, kCoarseBins);
+  G::sync();
+  for (uint32_t q = G::rank(); q < c2; q += G::kThreads) {
+    int32_t i;
+    uint32_t d;
+    F.get(q, i, d);
+    smem_add(&view[coarse_bin(bits_from_desc(d), d)], 1u);
+  }
+  G::sync();
+  find_boundaries<G>(view, sc, kCoarseBins, 1, K, 0u);
+  if (G::rank() == 0) {
+    sl.tstar = sc.res_bin[0];
+    sl.e0 = (int32_t)sc.res_below[0];
+    sl.q0n = (int32_t)sc.res_cnt[0];
+  }
+  G::sync();
+  return true;
+}
+
 // Exact coarse recovery with the row resident in registers (section 5.5,
 // "Row-local exact": the short-row specialization keeps aligned score vectors
 // in registers across boundary construction and classification).
@@ -2172,7 +2240,14 @@ __device__ void persistent_row(const Params& p, int M, Slot& sl, Slot& nx, const
       sl.q0n = (int)sl.n_front;  // eq. 21: E0 = {}, Q0 = A(tau), k0 = K
     }
     G::sync();
-    if (exact) exact_recovery<G>(p, row, L, F, hist, sc, sl, out_row, queues);
+    if (exact) {
+      // the last cutoff Phase 2 tried (T1 when the band widened T0)
+      const bool band = tau1 > tau0;
+      if (kind != kNextSampled ||
+          !bounded_recovery<G>(p, row, L, F, hist, vhist, sc, sl, queues, band ? T1 : T0,
+                               band ? tau1 : tau0))
+        exact_recovery<G>(p, row, L, F, hist, sc, sl, out_row, queues);
+    }
   }
   // Phase 3 of this row and Phase 1 of the next: side by side when the
   // frontier is in shared memory; one after the other, each by the whole CTA,
@@ -2181,7 +2256,7 @@ __device__ void persistent_row(const Params& p, int M, Slot& sl, Slot& nx, const
   const bool split = !idle && sl.n_front <= F.cap;
   if (split) {
     if ((int)(threadIdx.x >> 5) < kRefineWarps) {
-      refine<R>(F, sl.n_front, (uint32_t)(K - sl.e0), hist, sc, sl, out_row, K, queues,
+      refine<R>(F, sl.n_front, (uint32_t)K - sl.n_out, hist, sc, sl, out_row, K, queues,
                 (uint32_t)(R::kWarps * kQueueWords));
       finish_row<R>(p, sl, out_row);
       if (threadIdx.x == 0) write_slot_trace(p, sl);
@@ -2190,7 +2265,7 @@ __device__ void persistent_row(const Params& p, int M, Slot& sl, Slot& nx, const
     }
   } else {
     if (!idle) {
-      refine<G>(F, sl.n_front, (uint32_t)(K - sl.e0), hist, sc, sl, out_row, K, queues,
+      refine<G>(F, sl.n_front, (uint32_t)K - sl.n_out, hist, sc, sl, out_row, K, queues,
                 (uint32_t)(G::kWarps * kQueueWords));
       finish_row<G>(p, sl, out_row);
       if (threadIdx.x == 0) write_slot_trace(p, sl);

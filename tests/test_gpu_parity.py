@@ -119,6 +119,46 @@ def test_forced_routes(family, dual):
 
 
 @pytest.mark.parametrize("family", SAMPLED_FAMILIES)
+@pytest.mark.parametrize("dual", [0, 1])
+def test_exact_recovery_after_a_short_phase2(family, dual):
+    # Phase 2 falls short of K (the view over-counts the largest scores) while
+    # the view shows the next coarse bins filled.  Row 0: those bins complete
+    # the Top-K; row 2: they complete it with one key to spare; row 1: they do
+    # not, and the whole row's coarse histogram decides.  Values, tau*, |E0|
+    # and |Q0| must match the oracle's full-row recovery on every row.
+    K, s, N = 64, 16, 8192
+    q0 = -(-3 * K // (2 * s))
+    q1 = -(-7 * K // (4 * s))
+    rng = np.random.default_rng(11)
+    base = rng.standard_normal(N).astype(np.float32)
+
+    def planted(r, near_on, near_off):
+        row = base.copy()
+        a = oracle.view_phase(r, s)
+        on = np.arange(a, N, s)
+        off = np.array([i for i in range(N) if i % s != a])
+        row[on[:q0]] = 100.0
+        row[on[q0:q1]] = 90.0
+        row[off[:30]] = 100.0
+        row[on[q1:q1 + near_on]] = 80.0
+        row[off[30:30 + near_off]] = 80.0
+        return row
+
+    X = np.stack([planted(0, 8, 60), planted(1, 8, 0), planted(2, 8, 20), base])
+    ke = np.full(4, N, np.int32)
+    out, tr, plan, ctr = run_gpu(X, ke, K, family=family, stride=s, dual=dual, splits=3)
+    compare_rows(X, ke, K, out)
+    assert_counters_zero(ctr)
+    _, tr_ref = oracle_trace_for_plan(X, ke, K, plan)
+    compare_trace(tr, tr_ref)
+    exact = 3 if dual else 4
+    assert tr[:, 0].tolist() == [exact, exact, exact, 1]
+    # E0: the 100s and the 90s; Q0: the 80s
+    assert tr[[0, 2], 6].tolist() == [37, 37]
+    assert tr[[0, 2], 7].tolist() == [68, 28]
+
+
+@pytest.mark.parametrize("family", SAMPLED_FAMILIES)
 def test_guess_source(family):
     M, N, K = 12, 20000, 512
     X = _rows(M, N, 5, "normal")
