@@ -273,6 +273,17 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
 constexpr uint32_t kL2Ahead = ETK_L2_AHEAD_KB * 1024u;
 constexpr uint32_t kL2Next = ETK_L2_NEXT_KB * 1024u;
 
+// Requests row[0, L) into L2 ahead of a pass over a row that one CTA reads
+// several times (one thread; 64 KB per request, 16-byte aligned range).
+__device__ __forceinline__ void prefetch_row_l2(const float* row, int L) {
+  const uintptr_t b = (reinterpret_cast<uintptr_t>(row) + 15u) & ~(uintptr_t)15u;
+  const uintptr_t e = (reinterpret_cast<uintptr_t>(row) + (uintptr_t)L * 4u) & ~(uintptr_t)15u;
+  for (uintptr_t a = b; a < e; a += 65536u) {
+    const uintptr_t len = e - a < 65536u ? e - a : 65536u;
+    prefetch_l2(reinterpret_cast<const void*>(a), (uint32_t)len);
+  }
+}
+
 // ----------------------------------------------------------------------------
 // Shared state
 // ----------------------------------------------------------------------------
@@ -304,7 +315,8 @@ struct Slot {
   uint32_t seg_c0, seg_cb;  // KV-split: this segment's counts
   int32_t is_last;
   uint32_t vcnt0;  // Phase 1: view entries in bins <= tau0
-  int32_t pad_[2];
+  uint32_t vcnt1;  // ... and in bins <= tau1
+  int32_t pad_;
 };
 
 struct Params {
@@ -1385,20 +1397,30 @@ __device__ void refine(const Frontier& F, uint32_t n, uint32_t k, uint32_t* hist
 
 // Over the keys d <= T in [qlo, qhi) of row[0, L), by group G: the histogram
 // of their digits (d - qlo) >> shift (when `hist` is not null), and each
-// thread's count, smallest and largest key (accumulated into cnt, mn, mx).
-// Four 256-bit loads per thread in flight, run-length merged adds.  No group
-// barrier.
+// thread's count, smallest and largest key and how many keys equal each
+// (accumulated into cnt, mn, mx, nmn, nmx).  Two 256-bit loads per thread in
+// flight, run-length merged adds.  No group barrier.
 template <class G>
 __device__ void scan_key_hist(const float* row, int L, uint32_t T, uint64_t qlo, uint64_t qhi,
                               int shift, uint32_t* hist, uint32_t& cnt, uint32_t& mn,
-                              uint32_t& mx) {
+                              uint32_t& mx, uint32_t& nmn, uint32_t& nmx) {
   const int tid = G::rank();
   const Span sp = aligned_span(row, 0, L);
   auto take = [&](uint32_t d) {
     if (d <= T && (uint64_t)d >= qlo && (uint64_t)d < qhi) {
       ++cnt;
-      mn = min(mn, d);
-      mx = max(mx, d);
+      if (d < mn) {
+        mn = d;
+        nmn = 1u;
+      } else if (d == mn) {
+        ++nmn;
+      }
+      if (d > mx) {
+        mx = d;
+        nmx = 1u;
+      } else if (d == mx) {
+        ++nmx;
+      }
       return true;
     }
     return false;
@@ -1436,73 +1458,16 @@ __device__ void scan_key_hist(const float* row, int L, uint32_t T, uint64_t qlo,
   }
 }
 
-// Commit pass over row[0, L) by group G: every key d <= T below commit_below
-// goes to the output, then the first `ties` keys equal to tie_key (ranked
-// through sl.n_keep).  Per thread and 8-score vector, the committed and tied
-// positions are bit masks; one warp scan ranks the ties and one places the
-// outputs, so a warp issues two atomics per vector step whatever it commits.
-// Ends with a group barrier.
-template <class G>
-__device__ void scan_commit(const float* row, int L, uint32_t T, uint64_t commit_below,
-                            uint32_t tie_key, uint32_t ties, Slot& sl, int32_t* out_row, int K) {
-  const int tid = G::rank(), lane = tid & 31;
-  if (tid == 0) sl.n_keep = 0u;
-  G::sync();
-  auto warp_excl = [&](uint32_t v, uint32_t& total) {
-    uint32_t incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(kFull, incl, o);
-      if (lane >= o) incl += y;
-    }
-    total = __shfl_sync(kFull, incl, 31);
-    return incl - v;
-  };
-  // whole warps: x[0..8) with positions i0 .. i0+7, valid below `nvalid`
-  auto step = [&](const uint32_t* x, int i0, int nvalid) {
-    uint32_t cm = 0u, tm = 0u;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const uint32_t d = desc_key(x[e]);
-      const bool ok = e < nvalid && d <= T;
-      if (ok && (uint64_t)d < commit_below)
-        cm |= 1u << e;
-      else if (ok && ties > 0u && d == tie_key)
-        tm |= 1u << e;
-    }
-    if (tm != 0u && *(volatile uint32_t*)&sl.n_keep >= ties) tm = 0u;  // ties complete
-    if (__ballot_sync(kFull, (cm | tm) != 0u) == 0u) return;
-    if (__ballot_sync(kFull, tm != 0u) != 0u) {
-      uint32_t tt;
-      const uint32_t tex = warp_excl((uint32_t)__popc(tm), tt);
-      uint32_t base = 0u;
-      if (lane == 0) base = atomicAdd(&sl.n_keep, tt);
-      base = __shfl_sync(kFull, base, 0);
-      // keep the ties ranked below `ties`
-      uint32_t rank = base + tex;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        if (tm & (1u << e)) {
-          if (rank >= ties) tm &= ~(1u << e);
-          ++rank;
-        }
-      }
-    }
-    const uint32_t m = cm | tm;
-    uint32_t tot;
-    const uint32_t ex = warp_excl((uint32_t)__popc(m), tot);
-    uint32_t base = 0u;
-    if (lane == 0 && tot) base = atomicAdd(&sl.n_out, tot);
-    base = __shfl_sync(kFull, base, 0);
-    uint32_t slot = base + ex;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      if (m & (1u << e)) {
-        if (slot < (uint32_t)K) out_row[slot] = i0 + e;
-        ++slot;
-      }
-    }
-  };
+// Visits row[0, L) by group G one 8-score vector per thread and step, two
+// vectors per thread in flight: step(x, i0, nvalid) gets the bit patterns of
+// positions i0 .. i0 + nvalid - 1 (whole warps call it together; the
+// unaligned head and tail come first, one score per lane of warp 0).  Before
+// each step of two vectors the warp asks stop() (warp-uniform) whether the
+// rest of the row can be skipped.  No group barrier.
+template <class G, class Step, class Stop>
+__device__ __forceinline__ void visit_row(const float* row, int L, const Step& step,
+                                          const Stop& stop) {
+  const int tid = G::rank();
   const Span sp = aligned_span(row, 0, L);
   const int head = sp.a0, tail = L - sp.a_end;
   if (tid < 32) {  // the scalar head and tail (at most 14 scores), one lane each
@@ -1518,6 +1483,7 @@ __device__ void scan_commit(const float* row, int L, uint32_t T, uint64_t commit
   constexpr int kV = 2;  // vectors per thread in flight
   const int nvr = (sp.nvec + 31) & ~31;
   for (int t0 = 0; t0 < nvr; t0 += kV * G::kThreads) {
+    if (t0 + 32 * (tid >> 5) >= nvr || stop()) break;  // warp-uniform
     uint32_t x[kV][8];
 #pragma unroll
     for (int k = 0; k < kV; ++k) {
@@ -1536,6 +1502,90 @@ __device__ void scan_commit(const float* row, int L, uint32_t T, uint64_t commit
       step(x[k], sp.a0 + 8 * v, v < sp.nvec ? 8 : 0);
     }
   }
+}
+
+// Exclusive warp scan of v; `total` gets the warp's sum.
+__device__ __forceinline__ uint32_t warp_excl_scan(uint32_t v, uint32_t& total) {
+  const int lane = threadIdx.x & 31;
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  total = __shfl_sync(kFull, incl, 31);
+  return incl - v;
+}
+
+// Places the positions i0 + e (bits e of m) at consecutive output slots from
+// the warp's share of *n_out (one atomic per warp); slots >= K are dropped.
+__device__ __forceinline__ void commit_mask(uint32_t m, int i0, uint32_t* n_out, int32_t* out_row,
+                                            int K) {
+  uint32_t tot;
+  const uint32_t ex = warp_excl_scan((uint32_t)__popc(m), tot);
+  if (tot == 0u) return;
+  uint32_t base = 0u;
+  if ((threadIdx.x & 31) == 0) base = atomicAdd(n_out, tot);
+  uint32_t slot = __shfl_sync(kFull, base, 0) + ex;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    if (m & (1u << e)) {
+      if (slot < (uint32_t)K) out_row[slot] = i0 + e;
+      ++slot;
+    }
+  }
+}
+
+// Commit pass over row[0, L) by group G: every key d <= T in [commit_lo,
+// commit_below) goes to the output, then the first `ties` keys equal to
+// tie_key (ranked through sl.n_keep).  Per thread and 8-score vector, the
+// committed and tied positions are bit masks; one warp scan ranks the ties
+// and one places the outputs.  The pass ends as soon as all K output slots
+// are taken (a row of ties stops after its first K).  Ends with a group
+// barrier.
+template <class G>
+__device__ void scan_commit(const float* row, int L, uint32_t T, uint64_t commit_lo,
+                            uint64_t commit_below, uint32_t tie_key, uint32_t ties, Slot& sl,
+                            int32_t* out_row, int K) {
+  if (G::rank() == 0) {
+    sl.n_keep = 0u;
+    prefetch_row_l2(row, L);
+  }
+  G::sync();
+  auto step = [&](const uint32_t* x, int i0, int nvalid) {
+    uint32_t cm = 0u, tm = 0u;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const uint32_t d = desc_key(x[e]);
+      const bool ok = e < nvalid && d <= T;
+      if (ok && (uint64_t)d >= commit_lo && (uint64_t)d < commit_below)
+        cm |= 1u << e;
+      else if (ok && ties > 0u && d == tie_key)
+        tm |= 1u << e;
+    }
+    if (tm != 0u && *(volatile uint32_t*)&sl.n_keep >= ties) tm = 0u;  // ties complete
+    if (__ballot_sync(kFull, (cm | tm) != 0u) == 0u) return;
+    if (__ballot_sync(kFull, tm != 0u) != 0u) {
+      uint32_t tt;
+      const uint32_t tex = warp_excl_scan((uint32_t)__popc(tm), tt);
+      uint32_t base = 0u;
+      if ((threadIdx.x & 31) == 0) base = atomicAdd(&sl.n_keep, tt);
+      // keep the ties ranked below `ties`
+      uint32_t rank = __shfl_sync(kFull, base, 0) + tex;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if (tm & (1u << e)) {
+          if (rank >= ties) tm &= ~(1u << e);
+          ++rank;
+        }
+      }
+    }
+    commit_mask(cm | tm, i0, &sl.n_out, out_row, K);
+  };
+  auto full = [&]() {
+    return __shfl_sync(kFull, *(volatile uint32_t*)&sl.n_out, 0) >= (uint32_t)K;
+  };
+  visit_row<G>(row, L, step, full);
   G::sync();
 }
 
@@ -1806,11 +1856,13 @@ __device__ void view_cutoffs(const Params& p, const uint32_t* hist, GroupScratch
       } else {
         sl.T1 = t;
         sl.tau1 = b;
+        sl.vcnt1 = b >= 0 ? sc.res_below[1] + sc.res_cnt[1] : 0u;
       }
     }
   } else if (warp == 1 && G::rank() == 32) {
     sl.T1 = 0u;
     sl.tau1 = -1;
+    sl.vcnt1 = 0u;
   }
   G::sync();
 }
@@ -2076,12 +2128,32 @@ constexpr int kNextSampled = 1;  // view cutoffs T0 (and T1) in the slot
 constexpr int kNextDirect = 2;   // view too small: exact coarse recovery
 constexpr int kNextGuess = 3;    // guess-source cutoff T0 in the slot
 constexpr int kNextDeferred = 4; // handed to the heavy-row kernel (record in Params::defer)
+// Slot::route of a row handed to the heavy-row epilogue after its Phase 2 count.
+constexpr int kRouteDeferred = -1;
 
 // A sampled row whose view predicts C(tau0) ~ s * (view entries in bins <=
-// tau0) above eight on-chip frontier capacities: a tie group or a constant
-// row admitted whole.
-__device__ __forceinline__ bool heavy_view(const Params& p, const Slot& nx) {
-  return p.defer != nullptr && (uint64_t)nx.vcnt0 * (uint64_t)p.s > 8ull * (uint64_t)p.cap;
+// tau0) above four on-chip frontier capacities: a tie group, a constant row
+// or a block of subnormals admitted whole.  Such a frontier costs as much to
+// write and re-read as the row, and refining it in global memory takes more
+// rounds than the passes over the row the heavy-row machinery makes.
+__device__ __forceinline__ bool heavy_view(const Params& p, uint32_t vcnt) {
+  return p.defer != nullptr && (uint64_t)vcnt * (uint64_t)p.s > 4ull * (uint64_t)p.cap;
+}
+
+// Hands row nr to the heavy-row epilogue of this CTA (one thread): its record
+// {row, L, T0, T1, tau0, tau1} and its place in the CTA's list.
+__device__ __forceinline__ void defer_row(const Params& p, uint32_t* own, int nr, int L, uint32_t T0,
+                                          uint32_t T1, int tau0, int tau1) {
+  const int i = atomicAdd(p.counters + kCtrDeferred, 1);
+  int32_t* rec = p.defer + 8 * (int64_t)i;
+  rec[0] = nr;
+  rec[1] = L;
+  rec[2] = (int32_t)T0;
+  rec[3] = (int32_t)T1;
+  rec[4] = tau0;
+  rec[5] = tau1;
+  own[1 + own[0]] = (uint32_t)i;
+  own[0] = own[0] + 1u;
 }
 
 // Claims a row (or takes `assigned`) and runs its Phase 1 by group V into
@@ -2129,22 +2201,11 @@ __device__ void prepare_row(const Params& p, int M, int assigned, Slot& nx, uint
         // this CTA's list of deferred rows (persistent layout)
         uint32_t* own = reinterpret_cast<uint32_t*>(
             smem_base() + smem_layout(EXACT_TOPK_FAMILY_PERSISTENT_SAMPLED, kPersistentCap).own);
-        if (heavy_view(p, nx) && own[0] < kMaxOwnDeferred) {
+        if (heavy_view(p, nx.vcnt0) && own[0] < kMaxOwnDeferred) {
           // the rest of this row's method runs in the CTA's epilogue
           // (finish_deferred), after its other rows
           V::sync();  // every thread has read own[0]
-          if (V::rank() == 0) {
-            const int i = atomicAdd(p.counters + kCtrDeferred, 1);
-            int32_t* rec = p.defer + 8 * (int64_t)i;
-            rec[0] = nr;
-            rec[1] = L;
-            rec[2] = (int32_t)nx.T0;
-            rec[3] = (int32_t)nx.T1;
-            rec[4] = nx.tau0;
-            rec[5] = nx.tau1;
-            own[1 + own[0]] = (uint32_t)i;
-            own[0] = own[0] + 1u;
-          }
+          if (V::rank() == 0) defer_row(p, own, nr, L, nx.T0, nx.T1, nx.tau0, nx.tau1);
           kind = kNextDeferred;
         }
       } else {
@@ -2190,6 +2251,7 @@ __device__ void persistent_row(const Params& p, int M, Slot& sl, Slot& nx, const
     sl.c1 = -1;
     sl.tstar = -1;
     sl.e0 = 0;
+    sl.vcnt1 = kind == kNextSampled ? nx.vcnt1 : 0u;
   }
   __syncthreads();  // every thread has read nx; the next row's group may overwrite it
   if (kind == kNextPad) {
@@ -2217,14 +2279,25 @@ __device__ void persistent_row(const Params& p, int M, Slot& sl, Slot& nx, const
       if (c0 >= (uint32_t)K) {
         route = EXACT_TOPK_ROUTE_PRIMARY;
       } else if (p.dual) {
-        // Band rescue (eqs. 18-19): a second pass appends only T0 < d <= T1.
-        if (T1 > T0)
-          scan_two_class<G>(row, 0, L, T0, T1, true, &sl.n_drop, &sl.n_front, queues, drop,
-                            front_sink);
-        G::sync();
-        const uint32_t c1 = sl.n_front;
-        route = c1 >= (uint32_t)K ? EXACT_TOPK_ROUTE_BAND : EXACT_TOPK_ROUTE_EXACT_AFTER_BAND;
-        if (threadIdx.x == 0) sl.c1 = (int)c1;
+        uint32_t* own = reinterpret_cast<uint32_t*>(
+            smem_base() + smem_layout(EXACT_TOPK_FAMILY_PERSISTENT_SAMPLED, kPersistentCap).own);
+        if (heavy_view(p, sl.vcnt1) && own[0] < kMaxOwnDeferred) {
+          // the view puts the band far beyond on-chip capacity: the rest of
+          // the row's method runs in the CTA's epilogue (which counts C(tau0)
+          // again)
+          G::sync();  // every thread has read own[0]
+          if (threadIdx.x == 0) defer_row(p, own, r, L, T0, T1, tau0, tau1);
+          route = kRouteDeferred;
+        } else {
+          // Band rescue (eqs. 18-19): a second pass appends only T0 < d <= T1.
+          if (T1 > T0)
+            scan_two_class<G>(row, 0, L, T0, T1, true, &sl.n_drop, &sl.n_front, queues, drop,
+                              front_sink);
+          G::sync();
+          const uint32_t c1 = sl.n_front;
+          route = c1 >= (uint32_t)K ? EXACT_TOPK_ROUTE_BAND : EXACT_TOPK_ROUTE_EXACT_AFTER_BAND;
+          if (threadIdx.x == 0) sl.c1 = (int)c1;
+        }
       } else {
         route = EXACT_TOPK_ROUTE_EXACT_NO_BAND;
       }
@@ -2253,7 +2326,8 @@ __device__ void persistent_row(const Params& p, int M, Slot& sl, Slot& nx, const
   // frontier is in shared memory; one after the other, each by the whole CTA,
   // when it spilled (refinement then streams the global slice and wants every
   // warp) or when there is nothing to refine.
-  const bool split = !idle && sl.n_front <= F.cap;
+  const bool busy = !idle && sl.route != kRouteDeferred;  // a row deferred at its band: none
+  const bool split = busy && sl.n_front <= F.cap;
   if (split) {
     if ((int)(threadIdx.x >> 5) < kRefineWarps) {
       refine<R>(F, sl.n_front, (uint32_t)K - sl.n_out, hist, sc, sl, out_row, K, queues,
@@ -2264,7 +2338,7 @@ __device__ void persistent_row(const Params& p, int M, Slot& sl, Slot& nx, const
       prepare_row<V>(p, M, -1, nx, vhist, sc2[1], vd);
     }
   } else {
-    if (!idle) {
+    if (busy) {
       refine<G>(F, sl.n_front, (uint32_t)K - sl.n_out, hist, sc, sl, out_row, K, queues,
                 (uint32_t)(G::kWarps * kQueueWords));
       finish_row<G>(p, sl, out_row);
@@ -3437,82 +3511,154 @@ __global__ void __launch_bounds__(kFloorThreads) stream_floor_kernel(const float
 // group or a constant row admitted whole, the |Q0| = L worst case of section
 // 4.4) are set aside by the persistent CTA that claimed them and finished in
 // its epilogue, after its other rows, without materializing the frontier: the
-// counts of eqs. 16-19, the exact coarse recovery of eq. 20 when they fall
-// short, and the digit rounds of eqs. 22-25 all run as histogram passes over
-// the row itself, and one final pass commits the keys below the threshold and
-// the first ties (eq. 25).  The routes and trace fields are those of the
-// frontier method.
+// counts of eqs. 16-19 and the exact coarse recovery of eq. 20 when they fall
+// short run as passes over the row itself, and so do the digit rounds of eqs.
+// 22-25 until the keys left in play fit the on-chip frontier or are all equal
+// (eq. 25's ties).  The routes and trace fields are those of the frontier
+// method.
 
-// Count, smallest and largest of the keys d <= T in [qlo, qhi) of the row,
-// and (hist not null) their digit histogram from a clear one; block-wide
-// results, valid for every thread on return.
+// Count, extremes and their multiplicities of a set of keys.
+struct RowStats {
+  uint32_t cnt, kmin, kmax, nmin, nmax;
+};
+
+// Count, smallest and largest of the keys d <= T in [qlo, qhi) of the row and
+// how many keys equal each, and (hist not null) their digit histogram from a
+// clear one; block-wide results, valid for every thread on return.
 template <class G>
 __device__ void row_pass(const float* row, int L, uint32_t T, uint64_t qlo, uint64_t qhi,
-                         int shift, int nbins, uint32_t* hist, GroupScratch& sc, uint32_t& cnt,
-                         uint32_t& kmin, uint32_t& kmax) {
+                         int shift, int nbins, uint32_t* hist, GroupScratch& sc, RowStats& st) {
   G::sync();  // hist and the scratch are free
   if (hist != nullptr) clear_hist<G>(hist, nbins);
-  if (G::rank() == 0) sc.bcast = 0;
+  if (G::rank() == 0) {
+    sc.bcast = 0;
+    sc.res_cnt[0] = 0u;
+    sc.res_cnt[1] = 0u;
+    prefetch_row_l2(row, L);
+  }
   G::sync();
-  uint32_t c = 0u, mn = 0xFFFFFFFFu, mx = 0u;
-  scan_key_hist<G>(row, L, T, qlo, qhi, shift, hist, c, mn, mx);
+  uint32_t c = 0u, mn = 0xFFFFFFFFu, mx = 0u, nmn = 0u, nmx = 0u;
+  scan_key_hist<G>(row, L, T, qlo, qhi, shift, hist, c, mn, mx, nmn, nmx);
   c = __reduce_add_sync(kFull, c);
   if ((G::rank() & 31) == 0 && c) atomicAdd(&sc.bcast, (int)c);
+  uint32_t kmin, kmax;
   block_min_max<G>(mn, mx, sc, kmin, kmax);  // ends with a group barrier
-  cnt = (uint32_t)sc.bcast;
+  const uint32_t a = __reduce_add_sync(kFull, mn == kmin ? nmn : 0u);
+  const uint32_t b = __reduce_add_sync(kFull, mx == kmax ? nmx : 0u);
+  if ((G::rank() & 31) == 0) {
+    if (a) atomicAdd(&sc.res_cnt[0], a);
+    if (b) atomicAdd(&sc.res_cnt[1], b);
+  }
+  G::sync();
+  st = RowStats{(uint32_t)sc.bcast, kmin, kmax, sc.res_cnt[0], sc.res_cnt[1]};
 }
 
-// The k smallest keys among the keys d <= T of the row, all in [kmin, kmax]:
-// each round histograms an 11-bit digit over the interval left in play,
-// narrows it to the bucket holding the k-th key, and in the same pass
-// measures the range of the keys in play, so that a range of one value ends
-// the rounds with k ties (eq. 25).  The threshold is the one eqs. 22-25 reach.
+// Final pass of the heavy-row selection when the keys in play fit the shared
+// frontier: every key d <= T below qlo goes to the output, every key in [qlo,
+// qhi) to the frontier (positions through sl.n_keep).  Ends with a group
+// barrier.
 template <class G>
-__device__ Cut row_radix(const float* row, int L, uint32_t T, uint32_t k, uint32_t kmin,
-                         uint32_t kmax, uint32_t* hist, GroupScratch& sc) {
-  Cut cut{0, 0u, 0u, false};
-  uint64_t qlo = kmin, qhi = (uint64_t)kmax + 1u;  // keys in play
-  for (int round = 0; round < 6; ++round) {
-    if (kmin > kmax) break;  // nothing in play: inconsistent counts
-    if (kmin == kmax) {
-      cut.commit_below = kmin;  // every key in play equal: k ties
-      cut.tie_key = kmin;
-      cut.ties = k;
-      return cut;
+__device__ void collect_pass(const float* row, int L, uint32_t T, uint64_t qlo, uint64_t qhi,
+                             const Frontier& F, Slot& sl, int32_t* out_row, int K) {
+  G::sync();  // the frontier is free
+  if (G::rank() == 0) {
+    sl.n_keep = 0u;
+    prefetch_row_l2(row, L);
+  }
+  G::sync();
+  auto step = [&](const uint32_t* x, int i0, int nvalid) {
+    uint32_t cm = 0u, qm = 0u;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const uint32_t d = desc_key(x[e]);
+      const bool ok = e < nvalid && d <= T;
+      if (ok && (uint64_t)d < qlo)
+        cm |= 1u << e;
+      else if (ok && (uint64_t)d < qhi)
+        qm |= 1u << e;
     }
-    // the measured range narrows the interval
-    if ((uint64_t)kmin > qlo) qlo = kmin;
-    if ((uint64_t)kmax + 1u < qhi) qhi = (uint64_t)kmax + 1u;
+    if (__ballot_sync(kFull, cm != 0u) != 0u) commit_mask(cm, i0, &sl.n_out, out_row, K);
+    if (__ballot_sync(kFull, qm != 0u) != 0u) {
+      uint32_t tot;
+      const uint32_t ex = warp_excl_scan((uint32_t)__popc(qm), tot);
+      uint32_t base = 0u;
+      if ((threadIdx.x & 31) == 0) base = atomicAdd(&sl.n_keep, tot);
+      uint32_t pos = __shfl_sync(kFull, base, 0) + ex;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if (qm & (1u << e)) {
+          if (pos < F.cap) F.s[pos] = make_uint2((uint32_t)(i0 + e), desc_key(x[e]));
+          ++pos;
+        }
+      }
+    }
+  };
+  visit_row<G>(row, L, step, []() { return false; });
+  G::sync();
+}
+
+// Phase 3 over the row itself (eqs. 22-25): the k smallest of the keys in
+// play, the keys d <= T in [st.kmin, st.kmax] that `st` describes, every key
+// d <= T below them taken whole.  Each step first tries to close the
+// selection from the counts alone: k or more keys equal the smallest (k
+// ties, eq. 25), or fewer than k lie below the largest (all of them, then
+// ties at the largest); both end with one commit pass.  Keys in play that fit
+// the shared frontier are collected by one pass and refined on chip.
+// Otherwise one pass histograms an 11-bit digit over their measured range,
+// the bucket holding the k-th key becomes the keys in play, and, unless it
+// closes the quota or fits on chip, one more pass measures it.  Returns false
+// on inconsistent counts.
+template <class G>
+__device__ bool heavy_select(const float* row, int L, uint32_t T, uint32_t k, RowStats st,
+                             uint32_t* hist, const Frontier& F, GroupScratch& sc, Slot& sl,
+                             int32_t* out_row, int K, uint32_t* scratch, uint32_t scap) {
+  for (int round = 0; round < 6; ++round) {
+    if (k == 0u || st.cnt < k || st.kmin > st.kmax) break;  // inconsistent counts
+    if (st.nmin >= k) {
+      scan_commit<G>(row, L, T, 0u, st.kmin, st.kmin, k, sl, out_row, K);
+      return true;
+    }
+    if (st.cnt - st.nmax < k) {
+      scan_commit<G>(row, L, T, 0u, st.kmax, st.kmax, k - (st.cnt - st.nmax), sl, out_row, K);
+      return true;
+    }
+    uint64_t qlo = st.kmin, qhi = (uint64_t)st.kmax + 1u;
+    if (st.cnt <= F.cap) {
+      collect_pass<G>(row, L, T, qlo, qhi, F, sl, out_row, K);
+      refine<G>(F, st.cnt, k, hist, sc, sl, out_row, K, scratch, scap);
+      return true;
+    }
     const int bits = 64 - __clzll((long long)(qhi - qlo - 1u));
     const int shift = bits > 11 ? bits - 11 : 0;
     const int nbins = (int)((((qhi - qlo - 1u) >> shift) + 1u + 127u) & ~127ull);
-    uint32_t c;
-    row_pass<G>(row, L, T, qlo, qhi, shift, nbins, hist, sc, c, kmin, kmax);
-    if (kmin == kmax) continue;  // one value left: ties (top of the loop)
+    RowStats hs;
+    row_pass<G>(row, L, T, qlo, qhi, shift, nbins, hist, sc, hs);
     find_boundaries<G>(hist, sc, nbins, 1, k, 0u);
     const int b = sc.res_bin[0];
-    const uint32_t below = sc.res_below[0], cnt = sc.res_cnt[0];
+    const uint32_t below = sc.res_below[0], bc = sc.res_cnt[0];
     if (b < 0) break;
     qlo += (uint64_t)b << shift;
     const uint64_t top = qlo + ((uint64_t)1 << shift);
     qhi = top < qhi ? top : qhi;
-    if (below + cnt == k) {
-      cut.commit_below = qhi;  // the bucket closes the quota
-      return cut;
+    if (below + bc == k) {
+      // the bucket closes the quota: everything below its top
+      scan_commit<G>(row, L, T, 0u, qhi, 0u, 0u, sl, out_row, K);
+      return true;
     }
     k -= below;
-    // the bucket's range is measured by the next round's pass
-    kmin = (uint32_t)qlo;
-    kmax = (uint32_t)(qhi - 1u);
-    if (qhi - qlo == 1u) continue;
+    if (bc <= F.cap) {
+      collect_pass<G>(row, L, T, qlo, qhi, F, sl, out_row, K);
+      refine<G>(F, bc, k, hist, sc, sl, out_row, K, scratch, scap);
+      return true;
+    }
+    row_pass<G>(row, L, T, qlo, qhi, 0, 0, nullptr, sc, st);  // the bucket's own counts
   }
-  cut.bad = true;
-  return cut;
+  return false;
 }
 
 template <class G>
 __device__ void heavy_row(const Params& p, const int32_t* rec, uint32_t* hist, GroupScratch& sc,
-                          Slot& sl) {
+                          Slot& sl, const Frontier& F, uint32_t* scratch, uint32_t scap) {
   const int r = rec[0], L = rec[1];
   const uint32_t T0 = (uint32_t)rec[2], T1 = (uint32_t)rec[3];
   const int tau0 = rec[4], tau1 = rec[5];
@@ -3524,8 +3670,9 @@ __device__ void heavy_row(const Params& p, const int32_t* rec, uint32_t* hist, G
     sl.n_keep = 0u;
   }
   // Phase 2 counts (eqs. 16-19) with the range of the admitted keys
-  uint32_t c0, kmin, kmax;
-  row_pass<G>(row, L, T0, 0u, (uint64_t)T0 + 1u, 0, 0, nullptr, sc, c0, kmin, kmax);
+  RowStats st;
+  row_pass<G>(row, L, T0, 0u, (uint64_t)T0 + 1u, 0, 0, nullptr, sc, st);
+  const uint32_t c0 = st.cnt;
   int route, c1 = -1, tstar = -1, e0 = 0, q0;
   uint32_t T = T0;
   bool ok = true;
@@ -3536,9 +3683,8 @@ __device__ void heavy_row(const Params& p, const int32_t* rec, uint32_t* hist, G
     route = EXACT_TOPK_ROUTE_EXACT_NO_BAND;
     q0 = 0;
     if (p.dual) {
-      uint32_t cb;
-      row_pass<G>(row, L, T1, 0u, (uint64_t)T1 + 1u, 0, 0, nullptr, sc, cb, kmin, kmax);
-      c1 = (int)cb;  // band rescue: C(tau1)
+      row_pass<G>(row, L, T1, 0u, (uint64_t)T1 + 1u, 0, 0, nullptr, sc, st);
+      c1 = (int)st.cnt;  // band rescue: C(tau1)
       route = c1 >= K ? EXACT_TOPK_ROUTE_BAND : EXACT_TOPK_ROUTE_EXACT_AFTER_BAND;
       T = T1;
       q0 = c1;
@@ -3548,6 +3694,7 @@ __device__ void heavy_row(const Params& p, const int32_t* rec, uint32_t* hist, G
       // bins below tau* (E0) are committed by the final pass, Q0 = bin tau*
       G::sync();
       clear_hist<G>(hist, 2048);
+      if (G::rank() == 0) prefetch_row_l2(row, L);
       G::sync();
       scan_coarse_hist<G>(row, 0, L, hist);
       G::sync();
@@ -3559,13 +3706,12 @@ __device__ void heavy_row(const Params& p, const int32_t* rec, uint32_t* hist, G
       exact_cutoffs<G>(sl, ok ? tstar : 0);
       T = sl.T1;
       const uint32_t lo = tstar > 0 ? sl.T0 + 1u : 0u;
-      uint32_t cq;
-      row_pass<G>(row, L, T, lo, (uint64_t)T + 1u, 0, 0, nullptr, sc, cq, kmin, kmax);
+      row_pass<G>(row, L, T, lo, (uint64_t)T + 1u, 0, 0, nullptr, sc, st);
     }
   }
-  Cut cut{0, 0u, 0u, true};
-  if (ok) cut = row_radix<G>(row, L, T, (uint32_t)(K - e0), kmin, kmax, hist, sc);
-  if (!cut.bad) scan_commit<G>(row, L, T, cut.commit_below, cut.tie_key, cut.ties, sl, out_row, K);
+  if (ok)
+    heavy_select<G>(row, L, T, (uint32_t)(K - e0), st, hist, F, sc, sl, out_row, K, scratch,
+                    scap);
   finish_row<G>(p, sl, out_row);
   if (G::rank() == 0) write_trace(p, r, route, tau0, tau1, (int)c0, c1, tstar, e0, q0);
 }
@@ -3580,9 +3726,13 @@ __device__ __noinline__ void finish_deferred(const Params& p) {
   uint32_t* hist = reinterpret_cast<uint32_t*>(sm + lay.hist);
   GroupScratch& sc = *reinterpret_cast<GroupScratch*>(sm + lay.scratch);
   Slot& sl = *reinterpret_cast<Slot*>(sm + lay.slots);
+  const Frontier F{reinterpret_cast<uint2*>(sm + lay.frontier), (uint32_t)kPersistentCap, nullptr,
+                   (uint32_t)kPersistentCap};
+  uint32_t* scratch = reinterpret_cast<uint32_t*>(sm + lay.queues);
   const uint32_t n = own[0];
   for (uint32_t j = 0; j < n; ++j) {
-    heavy_row<G>(p, p.defer + 8 * (int64_t)own[1 + j], hist, sc, sl);
+    heavy_row<G>(p, p.defer + 8 * (int64_t)own[1 + j], hist, sc, sl, F, scratch,
+                 (uint32_t)(G::kWarps * kQueueWords));
     __syncthreads();
   }
 }

@@ -536,19 +536,52 @@ def test_stream_floor_reads_exactly_the_valid_prefixes(splits):
             assert got[r, q] == exp, (r, q)
 
 
+@pytest.mark.parametrize("workers", [1, 0])
+def test_persistent_rows_deferred_at_their_band(workers):
+    # Two-level rows whose view holds just enough ones for tau0 (Phase 2 runs
+    # on chip) but not for tau1, whose bin then holds the whole row: such a
+    # row leaves its band to the heavy-row epilogue.  Fewer and more ones
+    # than K, mixed with ordinary rows.
+    M, N, K, s = 12, 100000, 512, 64
+    q0 = -(-3 * K // (2 * s))
+    rng = np.random.default_rng(515)
+    X = rng.standard_normal((M, N)).astype(np.float32)
+    ke = np.full(M, N, np.int32)
+    for r in range(0, M, 2):
+        a = oracle.view_phase(r, s)
+        on = np.arange(a, N, s)
+        off = np.setdiff1d(np.arange(N), on)
+        n = K + (r // 2) % 3 * 4 - 5  # K - 5, K - 1, K + 3
+        X[r] = 0.0
+        X[r, rng.permutation(on)[:q0]] = 1.0
+        X[r, rng.permutation(off)[:n - q0]] = 1.0
+    ke[4] = N - 3333
+    X[4, ke[4]:] = np.nan
+    out, tr, plan, ctr = run_gpu(X, ke, K, family=etk.FAMILY_PERSISTENT_SAMPLED, stride=s,
+                                 dual=1, workers=workers)
+    compare_rows(X, ke, K, out)
+    assert_counters_zero(ctr)
+    _, tr_ref = oracle_trace_for_plan(X, ke, K, plan)
+    compare_trace(tr, tr_ref)
+    # fewer ones than K: the band, run by the heavy-row epilogue; more: the
+    # primary route on chip; row 4 (cut short) is deferred at its Phase 1
+    assert tr[0:M:2, 0].tolist() == [2, 2, 1, 2, 2, 1]
+
+
 @pytest.mark.parametrize("workers", [1, 3, 0])
 def test_persistent_heavy_rows_deferred_and_overflowing(workers):
     # Rows whose view predicts a frontier far beyond on-chip capacity
-    # (constant, -inf, signed-zero, two-level and subnormal rows) are finished
-    # after the CTA's other rows, by passes over the row itself; on one worker
-    # more than its 63-entry list of such rows exist, and the rest take the
-    # frontier route.  Mixed with ordinary, padded and empty rows.
-    M, N, K = 90, 40000, 512
+    # (constant, -inf, signed-zero, two-level, subnormal and near-tie rows)
+    # are finished after the CTA's other rows, by passes over the row itself;
+    # on one worker more than its 63-entry list of such rows exist, and the
+    # rest take the frontier route.  Mixed with ordinary, padded and empty
+    # rows; lengths up to 100000 straddle the deferral threshold.
+    M, N, K = 140, 100000, 512
     rng = np.random.default_rng(4242)
     X = rng.standard_normal((M, N)).astype(np.float32)
     ke = rng.integers(K + 1, N + 1, M).astype(np.int32)
     for r in range(M):
-        kind = r % 6
+        kind = r % 7
         if kind == 0:
             X[r] = 0.75
         elif kind == 1:
@@ -561,6 +594,10 @@ def test_persistent_heavy_rows_deferred_and_overflowing(workers):
         elif kind == 4:  # subnormals of both signs: sign bit over a 23-bit mantissa
             X[r] = (rng.integers(1, 1 << 23, N).astype(np.uint32) |
                     (rng.integers(0, 2, N).astype(np.uint32) << np.uint32(31))).view(np.float32)
+        elif kind == 5:  # K - 10 ones over two adjacent values, each far beyond capacity
+            X[r] = np.where(rng.integers(0, 2, N) == 1, np.float32(0.5),
+                            np.nextafter(np.float32(0.5), np.float32(1.0)))
+            X[r, rng.permutation(N)[:K - 10]] = 1.0
     ke[5], ke[11], ke[17] = 0, K, 7
     for r in range(M):
         X[r, ke[r]:] = np.nan
