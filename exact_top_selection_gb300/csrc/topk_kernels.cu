@@ -1395,41 +1395,48 @@ __device__ void refine(const Frontier& F, uint32_t n, uint32_t k, uint32_t* hist
 // Phase 3 over the row itself (frontiers too large to hold)
 // ----------------------------------------------------------------------------
 
-// Over the keys d <= T in [qlo, qhi) of row[0, L), by group G: the histogram
-// of their digits (d - qlo) >> shift (when `hist` is not null), and each
-// thread's count, smallest and largest key and how many keys equal each
-// (accumulated into cnt, mn, mx, nmn, nmx).  Two 256-bit loads per thread in
-// flight, run-length merged adds.  No group barrier.
+// Over the keys d <= T in [qlo, qhi) of row[0, L), by group G: each thread's
+// count, smallest and largest key and how many keys equal each (accumulated
+// into cnt, mn, mx, nmn, nmx), and, when `hist` is not null, the histogram of
+// the digits (d - hlo) >> shift of those at or above hlo, with their count in
+// nh.  Two 256-bit loads per thread in flight; a thread's adds merge runs of
+// one digit across the whole pass.  No group barrier.
 template <class G>
 __device__ void scan_key_hist(const float* row, int L, uint32_t T, uint64_t qlo, uint64_t qhi,
-                              int shift, uint32_t* hist, uint32_t& cnt, uint32_t& mn,
-                              uint32_t& mx, uint32_t& nmn, uint32_t& nmx) {
+                              uint64_t hlo, int shift, uint32_t* hist, uint32_t& cnt,
+                              uint32_t& mn, uint32_t& mx, uint32_t& nmn, uint32_t& nmx,
+                              uint32_t& nh) {
   const int tid = G::rank();
   const Span sp = aligned_span(row, 0, L);
+  // keys in play: lo <= d <= hi, one unsigned offset compare; histogrammed:
+  // hl <= d <= hi
+  const uint64_t top = qhi == 0u ? 0u : (qhi - 1u < (uint64_t)T ? qhi - 1u : (uint64_t)T);
+  if (qhi == 0u || qlo > top) return;
+  const uint32_t lo = (uint32_t)qlo, span = (uint32_t)(top - qlo);
+  const bool hon = hist != nullptr && hlo <= top;
+  const uint32_t hl = (uint32_t)(hlo > qlo ? hlo : qlo), hspan = hon ? (uint32_t)(top - hl) : 0u;
+  RunHist rh;
   auto take = [&](uint32_t d) {
-    if (d <= T && (uint64_t)d >= qlo && (uint64_t)d < qhi) {
+    if (d - lo <= span) {
       ++cnt;
-      if (d < mn) {
+      if (d <= mn) {
+        nmn = d == mn ? nmn + 1u : 1u;
         mn = d;
-        nmn = 1u;
-      } else if (d == mn) {
-        ++nmn;
       }
-      if (d > mx) {
+      if (d >= mx) {
+        nmx = d == mx ? nmx + 1u : 1u;
         mx = d;
-        nmx = 1u;
-      } else if (d == mx) {
-        ++nmx;
       }
-      return true;
+      const uint32_t h = d - hl;
+      if (hon && h <= hspan) {
+        ++nh;
+        rh.add(hist, h >> shift);
+      }
     }
-    return false;
   };
   const int head = sp.a0, tail = L - sp.a_end;
-  if (tid < head + tail) {
-    const uint32_t d = desc_key(ld_stream1(row + (tid < head ? tid : sp.a_end + (tid - head))));
-    if (take(d) && hist != nullptr) smem_add(&hist[(uint32_t)(((uint64_t)d - qlo) >> shift)], 1u);
-  }
+  if (tid < head + tail)
+    take(desc_key(ld_stream1(row + (tid < head ? tid : sp.a_end + (tid - head)))));
   const float* body = row + sp.a0;
   constexpr int kV = 2;
   for (int t0 = 0; t0 < sp.nvec; t0 += kV * G::kThreads) {
@@ -1444,18 +1451,14 @@ __device__ void scan_key_hist(const float* row, int L, uint32_t T, uint64_t qlo,
         for (int e = 0; e < 8; ++e) x[k][e] = 0xFFFFFFFFu;
       }
     }
-    RunHist rh;
 #pragma unroll
     for (int k = 0; k < kV; ++k) {
       if (t0 + k * G::kThreads + tid >= sp.nvec) break;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const uint32_t d = desc_key(x[k][e]);
-        if (take(d) && hist != nullptr) rh.add(hist, (uint32_t)(((uint64_t)d - qlo) >> shift));
-      }
+      for (int e = 0; e < 8; ++e) take(desc_key(x[k][e]));
     }
-    if (hist != nullptr) rh.flush(hist);
   }
+  if (hon) rh.flush(hist);
 }
 
 // Visits row[0, L) by group G one 8-score vector per thread and step, two
@@ -3517,30 +3520,64 @@ __global__ void __launch_bounds__(kFloorThreads) stream_floor_kernel(const float
 // (eq. 25's ties).  The routes and trace fields are those of the frontier
 // method.
 
-// Count, extremes and their multiplicities of a set of keys.
+// Count, extremes and their multiplicities of a set of keys, and how many of
+// them a histogram holds.
 struct RowStats {
-  uint32_t cnt, kmin, kmax, nmin, nmax;
+  uint32_t cnt, kmin, kmax, nmin, nmax, nhist;
 };
 
+// A digit histogram of the keys in [hlo, ...) of a set: digit (d - hlo) >> shift
+// over nbins bins.
+struct DigitHist {
+  uint64_t hlo;
+  int shift, nbins;
+};
+
+// Digit histogram over the keys of coarse bin tau, [cutoff(tau - 1) + 1, T]
+// with T = cutoff(tau): 11 bits of the bin's key range.  Whole group; the
+// result is valid for every thread.
+template <class G>
+__device__ DigitHist bin_digits(int tau, uint32_t T, GroupScratch& sc) {
+  G::sync();  // the scratch is free
+  if (G::rank() < 32) {
+    const uint32_t lo = tau > 0 ? cutoff_fast_warp(tau - 1) + 1u : 0u;
+    if (G::rank() == 0) sc.bcast2 = (int32_t)lo;
+  }
+  G::sync();
+  DigitHist h;
+  h.hlo = (uint32_t)sc.bcast2;
+  const uint64_t w = (uint64_t)T + 1u - h.hlo;  // >= 1
+  const int bits = 64 - __clzll((long long)(w - 1u | 1u));
+  h.shift = bits > 11 ? bits - 11 : 0;
+  h.nbins = (int)((((w - 1u) >> h.shift) + 1u + 127u) & ~127ull);
+  return h;
+}
+
 // Count, smallest and largest of the keys d <= T in [qlo, qhi) of the row and
-// how many keys equal each, and (hist not null) their digit histogram from a
-// clear one; block-wide results, valid for every thread on return.
+// how many keys equal each, and (hist not null) the digit histogram `dh` of
+// those at or above dh.hlo from a clear one; block-wide results, valid for
+// every thread on return.
 template <class G>
 __device__ void row_pass(const float* row, int L, uint32_t T, uint64_t qlo, uint64_t qhi,
-                         int shift, int nbins, uint32_t* hist, GroupScratch& sc, RowStats& st) {
+                         const DigitHist& dh, uint32_t* hist, GroupScratch& sc, RowStats& st) {
   G::sync();  // hist and the scratch are free
-  if (hist != nullptr) clear_hist<G>(hist, nbins);
+  if (hist != nullptr) clear_hist<G>(hist, dh.nbins);
   if (G::rank() == 0) {
     sc.bcast = 0;
     sc.res_cnt[0] = 0u;
     sc.res_cnt[1] = 0u;
+    sc.res_below[0] = 0u;
     prefetch_row_l2(row, L);
   }
   G::sync();
-  uint32_t c = 0u, mn = 0xFFFFFFFFu, mx = 0u, nmn = 0u, nmx = 0u;
-  scan_key_hist<G>(row, L, T, qlo, qhi, shift, hist, c, mn, mx, nmn, nmx);
+  uint32_t c = 0u, mn = 0xFFFFFFFFu, mx = 0u, nmn = 0u, nmx = 0u, nh = 0u;
+  scan_key_hist<G>(row, L, T, qlo, qhi, dh.hlo, dh.shift, hist, c, mn, mx, nmn, nmx, nh);
   c = __reduce_add_sync(kFull, c);
-  if ((G::rank() & 31) == 0 && c) atomicAdd(&sc.bcast, (int)c);
+  nh = __reduce_add_sync(kFull, nh);
+  if ((G::rank() & 31) == 0) {
+    if (c) atomicAdd(&sc.bcast, (int)c);
+    if (nh) atomicAdd(&sc.res_below[0], nh);
+  }
   uint32_t kmin, kmax;
   block_min_max<G>(mn, mx, sc, kmin, kmax);  // ends with a group barrier
   const uint32_t a = __reduce_add_sync(kFull, mn == kmin ? nmn : 0u);
@@ -3550,7 +3587,7 @@ __device__ void row_pass(const float* row, int L, uint32_t T, uint64_t qlo, uint
     if (b) atomicAdd(&sc.res_cnt[1], b);
   }
   G::sync();
-  st = RowStats{(uint32_t)sc.bcast, kmin, kmax, sc.res_cnt[0], sc.res_cnt[1]};
+  st = RowStats{(uint32_t)sc.bcast, kmin, kmax, sc.res_cnt[0], sc.res_cnt[1], sc.res_below[0]};
 }
 
 // Final pass of the heavy-row selection when the keys in play fit the shared
@@ -3597,6 +3634,17 @@ __device__ void collect_pass(const float* row, int L, uint32_t T, uint64_t qlo, 
   G::sync();
 }
 
+// 11 digit bits over the keys [lo, hi].
+__device__ __forceinline__ DigitHist digits_over(uint64_t lo, uint64_t hi) {
+  DigitHist h;
+  h.hlo = lo;
+  const uint64_t w = hi + 1u - lo;  // >= 1
+  const int bits = 64 - __clzll((long long)(w - 1u | 1u));
+  h.shift = bits > 11 ? bits - 11 : 0;
+  h.nbins = (int)((((w - 1u) >> h.shift) + 1u + 127u) & ~127ull);
+  return h;
+}
+
 // Phase 3 over the row itself (eqs. 22-25): the k smallest of the keys in
 // play, the keys d <= T in [st.kmin, st.kmax] that `st` describes, every key
 // d <= T below them taken whole.  Each step first tries to close the
@@ -3604,15 +3652,17 @@ __device__ void collect_pass(const float* row, int L, uint32_t T, uint64_t qlo, 
 // ties, eq. 25), or fewer than k lie below the largest (all of them, then
 // ties at the largest); both end with one commit pass.  Keys in play that fit
 // the shared frontier are collected by one pass and refined on chip.
-// Otherwise one pass histograms an 11-bit digit over their measured range,
-// the bucket holding the k-th key becomes the keys in play, and, unless it
-// closes the quota or fits on chip, one more pass measures it.  Returns false
-// on inconsistent counts.
+// Otherwise a digit histogram of the keys in play (the one the last pass
+// built when `pre`, over [h.hlo, ...), else one more pass over their measured
+// range) gives the bucket holding the k-th key; the bucket closes the quota,
+// is collected, or becomes the keys in play, measured and histogrammed by one
+// pass.  Returns false on inconsistent counts.
 template <class G>
 __device__ bool heavy_select(const float* row, int L, uint32_t T, uint32_t k, RowStats st,
-                             uint32_t* hist, const Frontier& F, GroupScratch& sc, Slot& sl,
-                             int32_t* out_row, int K, uint32_t* scratch, uint32_t scap) {
-  for (int round = 0; round < 6; ++round) {
+                             DigitHist h, bool pre, uint32_t* hist, const Frontier& F,
+                             GroupScratch& sc, Slot& sl, int32_t* out_row, int K,
+                             uint32_t* scratch, uint32_t scap) {
+  for (int round = 0; round < 8; ++round) {
     if (k == 0u || st.cnt < k || st.kmin > st.kmax) break;  // inconsistent counts
     if (st.nmin >= k) {
       scan_commit<G>(row, L, T, 0u, st.kmin, st.kmin, k, sl, out_row, K);
@@ -3622,24 +3672,25 @@ __device__ bool heavy_select(const float* row, int L, uint32_t T, uint32_t k, Ro
       scan_commit<G>(row, L, T, 0u, st.kmax, st.kmax, k - (st.cnt - st.nmax), sl, out_row, K);
       return true;
     }
-    uint64_t qlo = st.kmin, qhi = (uint64_t)st.kmax + 1u;
     if (st.cnt <= F.cap) {
-      collect_pass<G>(row, L, T, qlo, qhi, F, sl, out_row, K);
+      collect_pass<G>(row, L, T, st.kmin, (uint64_t)st.kmax + 1u, F, sl, out_row, K);
       refine<G>(F, st.cnt, k, hist, sc, sl, out_row, K, scratch, scap);
       return true;
     }
-    const int bits = 64 - __clzll((long long)(qhi - qlo - 1u));
-    const int shift = bits > 11 ? bits - 11 : 0;
-    const int nbins = (int)((((qhi - qlo - 1u) >> shift) + 1u + 127u) & ~127ull);
-    RowStats hs;
-    row_pass<G>(row, L, T, qlo, qhi, shift, nbins, hist, sc, hs);
-    find_boundaries<G>(hist, sc, nbins, 1, k, 0u);
+    const uint32_t under = pre ? st.cnt - st.nhist : 0u;  // keys in play below the histogram
+    if (!pre || under >= k) {
+      h = digits_over(st.kmin, st.kmax);
+      row_pass<G>(row, L, T, st.kmin, (uint64_t)st.kmax + 1u, h, hist, sc, st);
+      pre = true;
+      continue;
+    }
+    find_boundaries<G>(hist, sc, h.nbins, 1, k - under, 0u);
     const int b = sc.res_bin[0];
-    const uint32_t below = sc.res_below[0], bc = sc.res_cnt[0];
     if (b < 0) break;
-    qlo += (uint64_t)b << shift;
-    const uint64_t top = qlo + ((uint64_t)1 << shift);
-    qhi = top < qhi ? top : qhi;
+    const uint32_t below = sc.res_below[0] + under, bc = sc.res_cnt[0];
+    const uint64_t qlo = h.hlo + ((uint64_t)b << h.shift);
+    uint64_t qhi = qlo + ((uint64_t)1 << h.shift);
+    if (qhi > (uint64_t)st.kmax + 1u) qhi = (uint64_t)st.kmax + 1u;
     if (below + bc == k) {
       // the bucket closes the quota: everything below its top
       scan_commit<G>(row, L, T, 0u, qhi, 0u, 0u, sl, out_row, K);
@@ -3651,7 +3702,10 @@ __device__ bool heavy_select(const float* row, int L, uint32_t T, uint32_t k, Ro
       refine<G>(F, bc, k, hist, sc, sl, out_row, K, scratch, scap);
       return true;
     }
-    row_pass<G>(row, L, T, qlo, qhi, 0, 0, nullptr, sc, st);  // the bucket's own counts
+    // the bucket becomes the keys in play: its counts and next digit in one pass
+    h = digits_over(qlo, qhi - 1u);
+    row_pass<G>(row, L, T, qlo, qhi, h, hist, sc, st);
+    pre = true;
   }
   return false;
 }
@@ -3669,9 +3723,12 @@ __device__ void heavy_row(const Params& p, const int32_t* rec, uint32_t* hist, G
     sl.n_out = 0u;
     sl.n_keep = 0u;
   }
-  // Phase 2 counts (eqs. 16-19) with the range of the admitted keys
+  // Phase 2 counts (eqs. 16-19) with the range of the admitted keys and a
+  // digit histogram of the keys in the cutoff's own coarse bin, where a heavy
+  // row's mass sits
   RowStats st;
-  row_pass<G>(row, L, T0, 0u, (uint64_t)T0 + 1u, 0, 0, nullptr, sc, st);
+  DigitHist dh = bin_digits<G>(tau0, T0, sc);
+  row_pass<G>(row, L, T0, 0u, (uint64_t)T0 + 1u, dh, hist, sc, st);
   const uint32_t c0 = st.cnt;
   int route, c1 = -1, tstar = -1, e0 = 0, q0;
   uint32_t T = T0;
@@ -3683,7 +3740,8 @@ __device__ void heavy_row(const Params& p, const int32_t* rec, uint32_t* hist, G
     route = EXACT_TOPK_ROUTE_EXACT_NO_BAND;
     q0 = 0;
     if (p.dual) {
-      row_pass<G>(row, L, T1, 0u, (uint64_t)T1 + 1u, 0, 0, nullptr, sc, st);
+      dh = bin_digits<G>(tau1, T1, sc);
+      row_pass<G>(row, L, T1, 0u, (uint64_t)T1 + 1u, dh, hist, sc, st);
       c1 = (int)st.cnt;  // band rescue: C(tau1)
       route = c1 >= K ? EXACT_TOPK_ROUTE_BAND : EXACT_TOPK_ROUTE_EXACT_AFTER_BAND;
       T = T1;
@@ -3706,12 +3764,13 @@ __device__ void heavy_row(const Params& p, const int32_t* rec, uint32_t* hist, G
       exact_cutoffs<G>(sl, ok ? tstar : 0);
       T = sl.T1;
       const uint32_t lo = tstar > 0 ? sl.T0 + 1u : 0u;
-      row_pass<G>(row, L, T, lo, (uint64_t)T + 1u, 0, 0, nullptr, sc, st);
+      dh = digits_over(lo, T);
+      row_pass<G>(row, L, T, lo, (uint64_t)T + 1u, dh, hist, sc, st);
     }
   }
   if (ok)
-    heavy_select<G>(row, L, T, (uint32_t)(K - e0), st, hist, F, sc, sl, out_row, K, scratch,
-                    scap);
+    heavy_select<G>(row, L, T, (uint32_t)(K - e0), st, dh, true, hist, F, sc, sl, out_row, K,
+                    scratch, scap);
   finish_row<G>(p, sl, out_row);
   if (G::rank() == 0) write_trace(p, r, route, tau0, tau1, (int)c0, c1, tstar, e0, q0);
 }
