@@ -228,8 +228,10 @@ int exact_topk_run(const exact_topk_plan* plan, const float* logits, const int32
  *     (about num_rows * max_kv_len * 8 bytes) exceed the array are rejected
  *     with EXACT_TOPK_ERR_WORKSPACE_TOO_SMALL.  Every argument is checked
  *     before anything is enqueued: a rejected call launches nothing.
- *   - The first call on a device sets up (the array's device address, device
- *     attributes, kernel attributes): make it before any stream capture.
+ *   - The first call on a device resolves the array's device address and the
+ *     device's attributes; later calls on that device reuse them.  The kernel's
+ *     attributes are set at the device's first launch of the KV-split family,
+ *     by this or any other entry point.
  *   - Each call enqueues a memset of the counter region and one kernel on
  *     `stream`; it calls no cudaMalloc, cudaFree or other allocating routine.
  *   - Every call on a device shares the one array, which keeps the previous
