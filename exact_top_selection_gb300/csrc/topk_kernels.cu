@@ -3193,7 +3193,34 @@ __global__ void __launch_bounds__(kClusterThreads, 2) cluster_split_kernel(Param
     };
     const uint4 none = make_uint4(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu);
     const int nh4r = (nh4 + 31) & ~31;
-    for (int t = tid; t < nh4r; t += G::kThreads) classify(t < nh4 ? st4[t] : none, t, t < nh4);
+    {
+      // The part held in shared memory: the indices of vectors with an
+      // admissible score go to a per-warp stack (in the private histogram,
+      // unused until the selection), and each 32 of them are classified with
+      // every lane busy instead of every vector step running the per-score
+      // work for the few lanes that have any.
+      uint32_t* wstack = hist + warp * 128;  // depth < 64
+      uint32_t qn = 0u;                      // warp-uniform
+      for (int t = tid; t < nh4r; t += G::kThreads) {
+        const bool adm = t < nh4 && scr1.any(st4[t]);
+        const uint32_t bal = __ballot_sync(kFull, adm);
+        if (adm) wstack[qn + (uint32_t)__popc(bal & lt)] = (uint32_t)t;
+        qn += (uint32_t)__popc(bal);
+        if (qn >= 32u) {
+          __syncwarp();
+          const uint32_t tt = wstack[qn - 32u + (uint32_t)lane];
+          __syncwarp();  // read before later pushes reuse the slots
+          qn -= 32u;
+          classify(st4[tt], (int)tt, true);
+        }
+      }
+      if (qn > 0u) {
+        __syncwarp();
+        const bool has = (uint32_t)lane < qn;
+        const uint32_t tt = has ? wstack[lane] : 0u;
+        classify(has ? st4[tt] : none, (int)tt, has);
+      }
+    }
     // the part read from global memory: four vectors per thread in flight
     const int ntail = nv4 - nh4;
     const int ntr = (ntail + 31) & ~31;
