@@ -80,7 +80,11 @@ typedef enum exact_topk_family {
      - otherwise persistent sampled. */
   EXACT_TOPK_FAMILY_AUTO = 0,
   /* One CTA owns a row for all three phases; rows are claimed from a device
-     queue in completion order (section 5.5, "Persistent sampled"). */
+     queue in completion order (section 5.5, "Persistent sampled").  A row
+     whose view predicts a frontier beyond four on-chip capacities (a tie
+     group, a constant row: section 4.4's |Q0| = L case) is finished after the
+     CTA's other rows by passes over the row itself, with the same routes and
+     trace. */
   EXACT_TOPK_FAMILY_PERSISTENT_SAMPLED = 1,
   /* P CTAs scan disjoint segments of one row; the last to arrive finishes the
      row (section 4.5 eqs. 26-27; section 5.5, "Sampled KV-split"). */
